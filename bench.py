@@ -1,0 +1,378 @@
+"""Benchmark: Qwen-Image-2.1 DiT sampler steps at 1024^2 (N = 4096 image tokens, L = 407).
+
+One bench step = one FlowMatch Euler step of the 40-step loop: a DiT pass through
+all 32 blocks (the first step of every image is the joint pass that captures the
+text K/V; the other 39 run the image rows over the stored text K/V) followed by the
+Euler update. K timed steps run images back to back from step 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). Under torchrun each rank runs an independent
+replica on its own GPU (the step has no exchange between images): weak scaling.
+The reference arm times the CPU oracle on this host's cores on a bounded sample
+(one block of the joint 1024^2 pass per bench step, scaled to 32 blocks).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "DiT steps/s at 1024² (N=4096,L=407); achieved bf16 TFLOPS vs tensor peak"
+CASE = synth.LOOP_1024
+STEPS_PER_IMAGE = 40
+H = W_ = 64
+N = H * W_
+L = CASE.L
+HIDDEN, FFN, BLOCKS = 4096, 12288, 32
+
+
+def step_flops(joint: bool) -> int:
+    """Algorithmic FLOPs of one DiT pass (GEMMs + attention), as in the oracle's accounting."""
+    R = L + N if joint else N
+    gemm = 2 * R * (4 * HIDDEN * HIDDEN + 3 * HIDDEN * FFN)
+    att = N * (N + L) * 4 * HIDDEN + (L * (L + 1) // 2 * 4 * HIDDEN if joint else 0)
+    return BLOCKS * (gemm + att)
+
+
+def gateup_flops(joint: bool) -> int:
+    R = L + N if joint else N
+    return 2 * R * HIDDEN * (2 * FFN)
+
+
+def launches_per_step(joint: bool) -> int:
+    # timestep embed + 3 GEMVs, image projection (+ text pre-norm + text GEMM),
+    # 5 kernels per block, output head, Euler update
+    return 4 + 1 + (2 if joint else 0) + 5 * BLOCKS + 1 + 1
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["bf16_tflops"], p.get("bf16_tflops_sustained"), p["hbm_gbs"], "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling (200 ms) during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        time.sleep(0.3)
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- oracle (CPU)
+
+
+def oracle_block_sample(samples: int, seed: int = CASE.seed):
+    """Time the oracle on `samples` joint-pass blocks at 1024^2; returns seconds per block."""
+    from oracle import dit as odit
+    from oracle import rope as orope
+    Wt = synth.Weights(seed=seed, nblocks=1)
+    bw = Wt.block(0)
+    x = synth.input_f32(seed, 90, (L + N, HIDDEN))
+    tc, ts, ic, is_ = orope.token_tables(L, H, W_)
+    cos, sin = np.concatenate([tc, ic]), np.concatenate([ts, is_])
+    mods = odit.row_mods(odit.modulation(Wt.glob, 0.5), odit.modulation(Wt.glob, 0.0), L, L + N)
+    times = []
+    for _ in range(samples):
+        t0 = time.perf_counter()
+        odit.block_forward(bw, x, mods, L, cos, sin, 32)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def cores_used() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    nsamp = args.warmup + args.steps
+    times = oracle_block_sample(nsamp)
+    timed = times[args.warmup:]
+    per_step = float(np.mean(timed)) * BLOCKS
+    value = 1.0 / per_step
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "1024^2 sampler step, N=4096, L=407 (dense joint pass)", "global_batch": 1,
+                   "seq_len": L + N, "parallelism": "none"},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores_used(), "kind": "oracle",
+                         "sample": f"one oracle block (numpy fp32) of the joint 1024^2 pass per bench step, "
+                                   f"x32 blocks; {len(timed)} timed samples"},
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+
+def gpu_weights(dit, seed, device):
+    """Random-init bf16 weights drawn on the device (seeded), N(0, 0.02)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+
+    def t(*shape):
+        return (torch.randn(*shape, generator=g, device=device, dtype=torch.float32) * 0.02).to(torch.bfloat16)
+
+    d = synth.FULL
+    dit.load_global({name: t(*shp(d)) for name, shp, _ in synth.GLOBAL_TENSORS})
+    for b in range(BLOCKS):
+        dit.load_block(b, {name: t(*shp(d)) for name, shp, _ in synth.BLOCK_TENSORS})
+    torch.cuda.synchronize()
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import diffusion_transformer_text_gb300 as qi
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    qi.build()
+    stream = torch.cuda.current_stream()
+
+    dit = qi.DiT(blocks=BLOCKS, L_max=L, N_max=N, device=local_rank)
+    gpu_weights(dit, CASE.seed * 1000 + rank, dev)
+
+    sig, ts = qi.flow_sigmas(STEPS_PER_IMAGE, N)
+    tvals = [float(np.float32(ts[i]) / np.float32(1000.0)) for i in range(STEPS_PER_IMAGE)]
+    tc, tsn, ic, isn = qi.rope_tables(L, H, W_)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234 + rank)
+    txt = torch.randn(L, HIDDEN, generator=g, device=dev)
+    z = torch.randn(64, H, W_, generator=g, device=dev)
+    x = qi.pack_noise(z)
+    x0 = x.clone()
+    vel = torch.empty(N, 64, device=dev)
+
+    def sampler_step(i):
+        k = i % STEPS_PER_IMAGE
+        if k == 0:
+            x.copy_(x0)
+            dit.step(x, txt, tvals[0], tc, tsn, ic, isn, vel=vel)
+        else:
+            dit.step_cached(x, L, tvals[k], ic, isn, vel=vel)
+        qi.euler_update(x, vel, float(sig[k]), float(sig[k + 1]))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # warm-up (its own image), then the timed images start at step 0
+    for i in range(args.warmup):
+        sampler_step(i)
+    torch.cuda.synchronize()
+    dit.check()
+
+    clocks = Clocks(local_rank)
+    dit.profile(True)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        sampler_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier()
+    prof = dit.profile_read()
+    dit.profile(False)
+    dit.check()
+    ms = e0.elapsed_time(e1)
+    ms_t = torch.tensor([ms], dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms = float(ms_t.item())
+
+    njoint = sum(1 for i in range(args.steps) if i % STEPS_PER_IMAGE == 0)
+    nimg = args.steps - njoint
+    flops = njoint * step_flops(True) + nimg * step_flops(False)
+    value = world * args.steps / (ms / 1e3)
+    tflops = world * flops / (ms / 1e3) / 1e12
+
+    # ---- end to end through the public API with host buffers
+    xh = torch.empty(N, 64, dtype=torch.float32).pin_memory()
+    xh.copy_(x0.cpu())
+    txth = txt.cpu().pin_memory()
+    tabs_h = [t.cpu().pin_memory() for t in (tc, tsn, ic, isn)]
+    txt_d = torch.empty_like(txt)
+    tabs_d = [torch.empty_like(t) for t in (tc, tsn, ic, isn)]
+
+    def e2e_step(i):
+        k = i % STEPS_PER_IMAGE
+        x.copy_(xh, non_blocking=True)
+        if k == 0:
+            txt_d.copy_(txth, non_blocking=True)
+            for d_, h_ in zip(tabs_d, tabs_h):
+                d_.copy_(h_, non_blocking=True)
+            dit.step(x, txt_d, tvals[0], *tabs_d, vel=vel)
+        else:
+            tabs_d[2].copy_(tabs_h[2], non_blocking=True)
+            tabs_d[3].copy_(tabs_h[3], non_blocking=True)
+            dit.step_cached(x, L, tvals[k], tabs_d[2], tabs_d[3], vel=vel)
+        qi.euler_update(x, vel, float(sig[k]), float(sig[k + 1]))
+        xh.copy_(x, non_blocking=True)
+
+    e2e_steps = args.steps
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e_t = torch.tensor([e2e_s], dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    e2e_s = float(e2e_t.item())
+    h2d = (N * 64 * 4 + 2 * N * 64 * 4) * e2e_steps + njoint * (L * HIDDEN * 4 + 2 * L * 64 * 4)
+    d2h = N * 64 * 4 * e2e_steps
+
+    peak_b, peak_s, hbm, peak_kind = peaks()
+    gu_ms, gu_n = prof["gateup_gemm"]
+    gu_flops = BLOCKS * (njoint * gateup_flops(True) + nimg * gateup_flops(False))
+    gu_tflops = gu_flops / (gu_ms / 1e3) / 1e12 if gu_ms > 0 else None
+    traffic = None
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            traffic = json.load(f).get("gateup_gemm_bytes_per_launch")
+    except Exception:
+        pass
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "1024^2 sampler steps: N=4096 image tokens, L=407 text rows, 32 blocks, "
+                               "40-step images back to back (step 0 joint + text K/V capture, 39 image-only)",
+                   "global_batch": world, "seq_len": L + N, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: 14.2 GB of weights stream through every step",
+                   "joint_steps": njoint, "image_only_steps": nimg},
+        "achieved_tflops": tflops,
+        "tflops_frac_of_peak": tflops / world / peak_b,
+        "gpu_launches": njoint * launches_per_step(True) + nimg * launches_per_step(False),
+        "roofline": {"kernel": "gate/up GEMM + SwiGLU epilogue (tcgen05)", "bound": "tensor",
+                     "achieved": gu_tflops, "peak": peak_b, "unit": "TFLOP/s",
+                     "frac": (gu_tflops / peak_b) if gu_tflops else None, "traffic": traffic,
+                     "peak_kind": f"{peak_kind} bf16 burst", "launches": gu_n,
+                     "avg_launch_ms": gu_ms / gu_n if gu_n else None},
+        "kernel_ms": {k: v[0] for k, v in prof.items()},
+        "e2e": {"value": world * e2e_steps / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": h2d / e2e_steps,
+                "d2h_bytes_per_step": d2h / e2e_steps},
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        times = oracle_block_sample(3)
+        per_step = float(np.mean(times[1:])) * BLOCKS
+        line["cpu_baseline"] = {"value": 1.0 / per_step, "unit": "steps/s", "cores": cores_used(),
+                                "kind": "oracle",
+                                "sample": "2 timed oracle blocks (numpy fp32, dense joint 1024^2 pass), x32 blocks"}
+    dit.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    rc = run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,416 @@
+// Persistent, warp-specialised tcgen05 GEMM for the DiT block's dense
+// contractions (QKV, out-projection, SwiGLU gate/up, down, text projection),
+// with the block's elementwise work fused into the epilogue.
+//
+// D[M, N] = A[M, K] * B[N, K]^T; A = bf16 activations, B = bf16 weights
+// ([out, in] row-major), fp32 accumulation in tensor memory.
+//
+// Roles per CTA (192 threads):
+//   warp 0     TMA producer: 128x64 A and 256x64 B tiles into a 4-stage ring
+//   warp 1     TMEM owner and MMA issuer (one thread): 4 x tcgen05.mma 128x256x16
+//              per stage, accumulating into one of two 256-column TMEM buffers
+//   warps 2-5  epilogue: each thread owns one accumulator row (TMEM lane),
+//              reads 32 columns at a time and applies the fused epilogue while
+//              the MMA warp fills the other TMEM buffer.
+//
+// Every GEMM row is computed the same way whatever M is (no split-K, fixed
+// K order), so a row's result does not depend on the other rows in the pass:
+// this is what makes the text K/V of a joint pass equal a text-only pass.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace qi {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;  // 16 KB
+constexpr int kBBytes = kBN * kBK * 2;  // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
+constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
+constexpr uint32_t kTmemCols = 512;  // two 256-column accumulators
+constexpr int kGroupN = 8;           // tiles sweep 8 column tiles per row tile for L2 reuse
+
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mt, int& nt) {
+  const int group = kGroupN * num_m;
+  const int g = t / group;
+  const int first_n = g * kGroupN;
+  const int gsz = min(kGroupN, num_n - first_n);
+  const int local = t - g * group;
+  mt = local / gsz;
+  nt = first_n + local % gsz;
+}
+
+__device__ __forceinline__ float row_rinv(const float* ssp, int row) {
+  const float4* p = reinterpret_cast<const float4*>(ssp + static_cast<size_t>(row) * kSspParts);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kSspParts / 4; ++i) {
+    const float4 v = p[i];
+    s += v.x;
+    s += v.y;
+    s += v.z;
+    s += v.w;
+  }
+  return rsqrtf(s * (1.0f / kHidden) + kEps);
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&v)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+    w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+    w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+    w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+    d[i] = w;
+  }
+}
+
+// ---------------------------------------------------------------- epilogues
+
+__device__ __forceinline__ void epi_qkv(const GemmParams& p, uint32_t taddr, int row, int n0) {
+  const bool valid = row < p.M;
+  float rinv = 0.f;
+  const float* cs = nullptr;
+  const float* sn = nullptr;
+  __nv_bfloat16* dst = nullptr;
+  const int section = n0 / kHidden;  // 0 Q, 1 K, 2 V
+  const int col_in = n0 - section * kHidden;
+  if (valid) {
+    rinv = row_rinv(p.ssp_in, row);
+    const bool text = row < p.n_text;
+    const size_t trow = text ? static_cast<size_t>(row) : static_cast<size_t>(row - p.n_text);
+    cs = (text ? p.txt_cos : p.img_cos) + trow * kRopeCols;
+    sn = (text ? p.txt_sin : p.img_sin) + trow * kRopeCols;
+    if (section == 0)
+      dst = p.q + static_cast<size_t>(row) * kHidden + col_in;
+    else
+      dst = (section == 1 ? p.k : p.v) + static_cast<size_t>(row + p.kv_row_off) * kHidden + col_in;
+  }
+#pragma unroll 1
+  for (int c = 0; c < kBN / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(taddr + c * 32, r);
+    tmem_ld_wait();
+    if (!valid) continue;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * rinv;
+    if (section < 2) {
+      // interleaved rotary: pair j = columns (2j, 2j+1) of the head, angle column j
+      const int j0 = ((col_in + c * 32) & (kHeadDim - 1)) >> 1;
+      float cv[16], sv[16];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 a = reinterpret_cast<const float4*>(cs + j0)[i];
+        const float4 b = reinterpret_cast<const float4*>(sn + j0)[i];
+        cv[4 * i] = a.x; cv[4 * i + 1] = a.y; cv[4 * i + 2] = a.z; cv[4 * i + 3] = a.w;
+        sv[4 * i] = b.x; sv[4 * i + 1] = b.y; sv[4 * i + 2] = b.z; sv[4 * i + 3] = b.w;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float a = v[2 * j], b = v[2 * j + 1];
+        v[2 * j] = a * cv[j] - b * sv[j];
+        v[2 * j + 1] = a * sv[j] + b * cv[j];
+      }
+    }
+    store_bf16x32(dst + c * 32, v);
+  }
+}
+
+__device__ __forceinline__ void epi_resid(const GemmParams& p, uint32_t taddr, int row, int n0) {
+  const bool valid = row < p.M;
+  const float* mrow = p.mod + (row < p.n_text ? kMod : 0);
+  const float* gate = mrow + p.gate_chunk * kHidden + n0;
+  const float* scale = mrow + p.scale_chunk * kHidden + n0;
+  float* xrow = p.x + static_cast<size_t>(row) * kHidden + n0;
+  __nv_bfloat16* arow = p.xa + static_cast<size_t>(row) * kHidden + n0;
+  float ss = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < kBN / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(taddr + c * 32, r);
+    tmem_ld_wait();
+    if (!valid) continue;
+    float xn[32], av[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int col = c * 32 + 4 * i;
+      float4 base;
+      if (p.resid_set) {
+        const uint2 bb = *reinterpret_cast<const uint2*>(p.bias + n0 + col);
+        base.x = __uint_as_float(bb.x << 16);
+        base.y = __uint_as_float(bb.x & 0xFFFF0000u);
+        base.z = __uint_as_float(bb.y << 16);
+        base.w = __uint_as_float(bb.y & 0xFFFF0000u);
+        xn[4 * i + 0] = __uint_as_float(r[4 * i + 0]) + base.x;
+        xn[4 * i + 1] = __uint_as_float(r[4 * i + 1]) + base.y;
+        xn[4 * i + 2] = __uint_as_float(r[4 * i + 2]) + base.z;
+        xn[4 * i + 3] = __uint_as_float(r[4 * i + 3]) + base.w;
+      } else {
+        base = *reinterpret_cast<const float4*>(xrow + col);
+        const float4 g = *reinterpret_cast<const float4*>(gate + col);
+        xn[4 * i + 0] = base.x + g.x * __uint_as_float(r[4 * i + 0]);
+        xn[4 * i + 1] = base.y + g.y * __uint_as_float(r[4 * i + 1]);
+        xn[4 * i + 2] = base.z + g.z * __uint_as_float(r[4 * i + 2]);
+        xn[4 * i + 3] = base.w + g.w * __uint_as_float(r[4 * i + 3]);
+      }
+      *reinterpret_cast<float4*>(xrow + col) = make_float4(xn[4 * i], xn[4 * i + 1], xn[4 * i + 2], xn[4 * i + 3]);
+      const float4 s = *reinterpret_cast<const float4*>(scale + col);
+      av[4 * i + 0] = xn[4 * i + 0] * (1.f + s.x);
+      av[4 * i + 1] = xn[4 * i + 1] * (1.f + s.y);
+      av[4 * i + 2] = xn[4 * i + 2] * (1.f + s.z);
+      av[4 * i + 3] = xn[4 * i + 3] * (1.f + s.w);
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) ss += xn[i] * xn[i];
+    store_bf16x32(arow + c * 32, av);
+  }
+  if (valid) p.ssp_out[static_cast<size_t>(row) * kSspParts + n0 / kBN] = ss;
+}
+
+__device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, int row, int n0) {
+  const bool valid = row < p.M;
+  const float rinv = valid ? row_rinv(p.ssp_in, row) : 0.f;
+  // tile columns [0,128) are gate rows 128j.., [128,256) the matching up rows
+  __nv_bfloat16* dst = p.h + static_cast<size_t>(row) * kFfn + (n0 / kBN) * (kBN / 2);
+#pragma unroll 1
+  for (int c = 0; c < kBN / 64; ++c) {
+    uint32_t g[32], u[32];
+    tmem_ld32(taddr + c * 32, g);
+    tmem_ld32(taddr + kBN / 2 + c * 32, u);
+    tmem_ld_wait();
+    if (!valid) continue;
+    float hv[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float a = __uint_as_float(g[i]) * rinv;
+      const float b = __uint_as_float(u[i]) * rinv;
+      hv[i] = a / (1.f + __expf(-a)) * b;
+    }
+    store_bf16x32(dst + c * 32, hv);
+  }
+}
+
+__device__ __forceinline__ void epi_f32(const GemmParams& p, uint32_t taddr, int row, int n0) {
+  const bool valid = row < p.M;
+  float* dst = p.d + static_cast<size_t>(row) * p.N + n0;
+#pragma unroll 1
+  for (int c = 0; c < kBN / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(taddr + c * 32, r);
+    tmem_ld_wait();
+    if (!valid) continue;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      reinterpret_cast<float4*>(dst + c * 32)[i] =
+          make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]), __uint_as_float(r[4 * i + 2]),
+                      __uint_as_float(r[4 * i + 3]));
+  }
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <int KIND>
+__global__ void __launch_bounds__(192, 1)
+    gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_m = (p.M + kBM - 1) / kBM;
+  const int num_n = p.N / kBN;
+  const int total = num_m * num_n;
+  const int kblocks = p.K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        if (*abort_flag) break;
+        int mt, nt;
+        tile_coords(t, num_m, num_n, mt, nt);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u)) {
+            report_error(p.err, kErrTimeoutProducer);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          tma_load_2d(sA + stage * kABytes, &tmA, &full[stage], kb * kBK, mt * kBM);
+          tma_load_2d(sB + stage * kBBytes, &tmB, &full[stage], kb * kBK, nt * kBN);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // every load this thread issued must land before the CTA may exit
+      for (int s = 0; s < kStages; ++s)
+        if ((issued_mask >> s) & 1u)
+          if (!mbar_wait(&full[s], (issued_parity >> s) & 1u)) report_error(p.err, kErrTimeoutDrain);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        if (*abort_flag) break;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u)) {
+          report_error(p.err, kErrTimeoutMma);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * kBN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase)) {
+            report_error(p.err, kErrTimeoutMma);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * kABytes);
+          const uint32_t b0 = smem_u32(sB + stage * kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16_ss(d, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k), kIdesc,
+                        (kb | k) != 0 ? 1u : 0u);
+          mma_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // all MMAs of this thread must finish before TMEM is released
+      mma_commit(drain);
+      if (!mbar_wait(drain, 0)) report_error(p.err, kErrTimeoutDrain);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5)
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_in_tile = quarter * 32 + lane;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      int mt, nt;
+      tile_coords(t, num_m, num_n, mt, nt);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase));
+      if (!ok) {
+        if (lane == 0) report_error(p.err, kErrTimeoutEpilogue);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN;
+      const int row = mt * kBM + row_in_tile;
+      if (KIND == kEpiQkv)
+        epi_qkv(p, taddr, row, nt * kBN);
+      else if (KIND == kEpiResid)
+        epi_resid(p, taddr, row, nt * kBN);
+      else if (KIND == kEpiSwiglu)
+        epi_swiglu(p, taddr, row, nt * kBN);
+      else
+        epi_f32(p, taddr, row, nt * kBN);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int KIND>
+cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
+                        cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  gemm_bf16_tc<KIND><<<grid, 192, kSmemBytes, stream>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                        int grid_ctas, cudaStream_t stream) {
+  if (p.M <= 0) return cudaSuccess;
+  if (p.N % kBN != 0 || p.K % kBK != 0) return cudaErrorInvalidValue;
+  const int tiles = ((p.M + kBM - 1) / kBM) * (p.N / kBN);
+  const int grid = tiles < grid_ctas ? tiles : grid_ctas;
+  switch (kind) {
+    case kEpiQkv:
+      return launch_kind<kEpiQkv>(a, b, p, grid, stream);
+    case kEpiResid:
+      return launch_kind<kEpiResid>(a, b, p, grid, stream);
+    case kEpiSwiglu:
+      return launch_kind<kEpiSwiglu>(a, b, p, grid, stream);
+    case kEpiF32:
+      return launch_kind<kEpiF32>(a, b, p, grid, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace qi

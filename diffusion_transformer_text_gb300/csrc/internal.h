@@ -1,0 +1,98 @@
+// Declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace qi {
+
+constexpr int kHidden = 4096;
+constexpr int kHeads = 32;
+constexpr int kHeadDim = 128;
+constexpr int kFfn = 12288;
+constexpr int kMod = 4 * kHidden;
+constexpr int kPatch = 64;
+constexpr int kTdim = 256;
+constexpr int kRopeCols = 64;
+constexpr float kEps = 1e-6f;
+
+// GEMM tile: 128 rows x 256 columns per CTA, K in steps of 64 (one 128-byte
+// swizzle span of bf16). Sum-of-squares partials are kept per 256-column tile.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kSspParts = kHidden / kBN;  // 16 partial sums per row
+
+enum EpiKind : int {
+  kEpiQkv = 0,     // row scale 1/rms, RoPE on Q and K, bf16 Q / K / V stores
+  kEpiResid = 1,   // residual update (+ gate) or bias set, bf16 modulated copy, sum of squares
+  kEpiSwiglu = 2,  // row scale 1/rms, silu(gate) * up, bf16 store
+  kEpiF32 = 3,     // plain fp32 store of D (test hook)
+};
+
+struct GemmParams {
+  int M, N, K;
+  int n_text;          // activation rows < n_text are text rows (t = 0 modulation row)
+  const float* mod;    // [2][kMod]: row 0 for the sampled t, row 1 for t = 0
+  const float* ssp_in; // [M][kSspParts] sum-of-squares partials of the GEMM's A rows
+  // kEpiQkv
+  __nv_bfloat16* q;
+  __nv_bfloat16* k;
+  __nv_bfloat16* v;
+  int kv_row_off;      // K/V store row = activation row + kv_row_off
+  const float* txt_cos;
+  const float* txt_sin;
+  const float* img_cos;
+  const float* img_sin;
+  // kEpiSwiglu
+  __nv_bfloat16* h;
+  // kEpiResid
+  float* x;                 // fp32 residual stream [M][kHidden]
+  __nv_bfloat16* xa;        // bf16(x * (1 + scale)) for the next GEMM
+  float* ssp_out;           // [M][kSspParts]
+  const uint16_t* bias;     // set mode: x = acc + bias
+  int resid_set;            // 1: x = acc + bias; 0: x += gate * acc
+  int gate_chunk;           // modulation chunk used as gate (0..3)
+  int scale_chunk;          // modulation chunk used as (1 + scale) for xa
+  float* d;                 // kEpiF32: D [M][N]
+  int* err;                 // device error word
+};
+
+// Launch one persistent tcgen05 GEMM D[M,N] = A[M,K] * B[N,K]^T with the
+// epilogue `kind`. A and B maps are 2-D bf16 maps with box {64, 128} / {64, 256}.
+cudaError_t launch_gemm(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                        int grid_ctas, cudaStream_t stream);
+
+struct AttnParams {
+  const __nv_bfloat16* q;  // [Rq][kHidden], query row r has global index r + q_off
+  const __nv_bfloat16* k;  // [Lk][kHidden], key rows 0..Lk-1 (text first)
+  const __nv_bfloat16* v;
+  __nv_bfloat16* o;        // [Rq][kHidden]
+  int Rq;
+  int q_off;
+  int L;                   // text rows: global index < L
+  int Lk;                  // keys visible to image rows
+};
+
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
+
+// Small kernels (kernels_small.cu)
+cudaError_t launch_timestep_embed(float t, float* e, cudaStream_t s);
+cudaError_t launch_gemv2(const float* x, int in_dim, const uint16_t* W, const uint16_t* b, int out_dim, float* y,
+                         int silu_in, cudaStream_t s);
+cudaError_t launch_txt_prenorm(const float* txt, int L, const uint16_t* w, __nv_bfloat16* out, cudaStream_t s);
+cudaError_t launch_img_in(const float* img, int N, const uint16_t* W, const uint16_t* b, const float* mod,
+                          float* x, __nv_bfloat16* xa, float* ssp, cudaStream_t s);
+cudaError_t launch_head(const float* x, int N, const float* ssp, const uint16_t* W, const uint16_t* b, float* vel,
+                        cudaStream_t s);
+cudaError_t launch_block_prep(const float* x, int R, int n_text, const float* mod, __nv_bfloat16* xa, float* ssp,
+                              cudaStream_t s);
+cudaError_t launch_euler(float* x, const float* vel, long long n, float s_i, float s_next, cudaStream_t s);
+cudaError_t launch_rope_axis(float theta, float* c0, float* s0, float* c1, float* s1, float* c2, float* s2,
+                             cudaStream_t s);
+cudaError_t launch_rope_tokens(int L, int h, int w, float theta, float* tc, float* ts, float* ic, float* is,
+                               cudaStream_t s);
+cudaError_t launch_pack_noise(const float* z, int h, int w, float* x, cudaStream_t s);
+
+}  // namespace qi

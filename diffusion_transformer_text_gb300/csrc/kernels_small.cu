@@ -1,0 +1,436 @@
+// The DiT step's small, memory-bound kernels: timestep embedding and the
+// shared modulation (GEMVs over 2 rows), text pre-norm, image-token projection,
+// output head, RoPE tables, noise packing and the Euler update.
+#include <math.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace qi {
+namespace {
+
+__device__ __forceinline__ float silu(float a) { return a / (1.f + expf(-a)); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---------------------------------------------------------------- timestep
+
+// e[0] = sinusoid of 1000*t, e[1] = sinusoid of 0; [cos(1000 t w_k) | sin(...)],
+// w_k = 10000^(-k/128), k < 128.
+__global__ void timestep_embed_kernel(float t, float* e) {
+  const int k = threadIdx.x;  // 0..127
+  const float w = powf(10000.f, -static_cast<float>(k) / 128.f);
+  const float a = (1000.f * t) * w;
+  e[k] = cosf(a);
+  e[128 + k] = sinf(a);
+  e[256 + k] = 1.f;  // cos(0)
+  e[256 + 128 + k] = 0.f;
+}
+
+// y[r][o] = W[o] . act(x[r]) + b[o] for r = 0, 1; act = silu or identity.
+// Each warp computes kOutPerWarp outputs; W rows are read once, 16 bytes per lane.
+constexpr int kOutPerWarp = 4;
+__global__ void __launch_bounds__(256) gemv2_kernel(const float* __restrict__ x, int in_dim,
+                                                    const uint16_t* __restrict__ W, const uint16_t* __restrict__ b,
+                                                    int out_dim, float* __restrict__ y, int silu_in) {
+  extern __shared__ float xs[];  // [2][in_dim]
+  for (int i = threadIdx.x; i < 2 * in_dim; i += blockDim.x) {
+    const float v = x[i];
+    xs[i] = silu_in ? silu(v) : v;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int o_base = (blockIdx.x * 8 + warp) * kOutPerWarp;
+  const int chunks = in_dim / 8;
+#pragma unroll 1
+  for (int j = 0; j < kOutPerWarp; ++j) {
+    const int o = o_base + j;
+    if (o >= out_dim) break;
+    const uint4* wr = reinterpret_cast<const uint4*>(W + static_cast<size_t>(o) * in_dim);
+    float a0 = 0.f, a1 = 0.f;
+    for (int c = lane; c < chunks; c += 32) {
+      const uint4 wv = wr[c];
+      const float* x0 = xs + c * 8;
+      const float* x1 = xs + in_dim + c * 8;
+      const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float lo = __uint_as_float(ws[q] << 16);
+        const float hi = __uint_as_float(ws[q] & 0xFFFF0000u);
+        a0 += lo * x0[2 * q] + hi * x0[2 * q + 1];
+        a1 += lo * x1[2 * q] + hi * x1[2 * q + 1];
+      }
+    }
+    a0 = warp_sum(a0);
+    a1 = warp_sum(a1);
+    if (lane == 0) {
+      const float bb = bf16_bits_to_float(b[o]);
+      y[o] = a0 + bb;
+      y[out_dim + o] = a1 + bb;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- norms
+
+__device__ __forceinline__ float block_sum_256(float v, float* red) {
+  v = warp_sum(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) s += red[i];
+  __syncthreads();
+  return s;
+}
+
+// ZeroCenterRMSNorm of text features: out = bf16(x / rms(x) * (1 + w)).
+__global__ void __launch_bounds__(256) txt_prenorm_kernel(const float* __restrict__ txt,
+                                                          const uint16_t* __restrict__ w,
+                                                          __nv_bfloat16* __restrict__ out) {
+  __shared__ float red[8];
+  const int row = blockIdx.x;
+  const float4* xr = reinterpret_cast<const float4*>(txt + static_cast<size_t>(row) * kHidden);
+  float4 v[4];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[i] = xr[threadIdx.x + 256 * i];
+    ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+  }
+  const float rinv = rsqrtf(block_sum_256(ss, red) * (1.f / kHidden) + kEps);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = 4 * (threadIdx.x + 256 * i);
+    const uint2 wb = *reinterpret_cast<const uint2*>(w + c);
+    const float g0 = 1.f + __uint_as_float(wb.x << 16), g1 = 1.f + __uint_as_float(wb.x & 0xFFFF0000u);
+    const float g2 = 1.f + __uint_as_float(wb.y << 16), g3 = 1.f + __uint_as_float(wb.y & 0xFFFF0000u);
+    uint2 o;
+    o.x = pack_bf16x2(v[i].x * rinv * g0, v[i].y * rinv * g1);
+    o.y = pack_bf16x2(v[i].z * rinv * g2, v[i].w * rinv * g3);
+    *reinterpret_cast<uint2*>(out + static_cast<size_t>(row) * kHidden + c) = o;
+  }
+}
+
+// For a residual stream given directly: xa = bf16(x * (1 + s1[row])), plus the
+// per-256-column sums of squares. One block per row; 16 consecutive columns per thread.
+__global__ void __launch_bounds__(256) block_prep_kernel(const float* __restrict__ x, int n_text,
+                                                         const float* __restrict__ mod,
+                                                         __nv_bfloat16* __restrict__ xa, float* __restrict__ ssp) {
+  const int row = blockIdx.x;
+  const float* mrow = mod + (row < n_text ? kMod : 0);  // s1 is chunk 0
+  const int c0 = threadIdx.x * 16;
+  const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(row) * kHidden + c0);
+  const float4* sr = reinterpret_cast<const float4*>(mrow + c0);
+  float ss = 0.f;
+  uint32_t packed[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 v = xr[i];
+    const float4 s = sr[i];
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    packed[2 * i] = pack_bf16x2(v.x * (1.f + s.x), v.y * (1.f + s.y));
+    packed[2 * i + 1] = pack_bf16x2(v.z * (1.f + s.z), v.w * (1.f + s.w));
+  }
+  uint4* dst = reinterpret_cast<uint4*>(xa + static_cast<size_t>(row) * kHidden + c0);
+  dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  // 16 threads cover one 256-column group
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 15) == 0) ssp[static_cast<size_t>(row) * kSspParts + threadIdx.x / 16] = ss;
+}
+
+// ---------------------------------------------------------------- image projection
+
+// x[r] = img[r] . W^T + b (64 -> 4096) for image rows (sampled-t modulation),
+// xa = bf16(x * (1 + s1)), ssp = per-256-column sums of squares.
+// Block: 256 columns (one per thread, its 64 weights in registers) x 64 rows.
+constexpr int kImgRows = 64;
+__global__ void __launch_bounds__(256) img_in_kernel(const float* __restrict__ img, int N,
+                                                     const uint16_t* __restrict__ W, const uint16_t* __restrict__ b,
+                                                     const float* __restrict__ mod, float* __restrict__ x,
+                                                     __nv_bfloat16* __restrict__ xa, float* __restrict__ ssp) {
+  __shared__ float rows[kImgRows][kPatch];
+  __shared__ float red[kImgRows][8];
+  const int col = blockIdx.x * 256 + threadIdx.x;
+  const int r0 = blockIdx.y * kImgRows;
+  const int nrows = min(kImgRows, N - r0);
+  for (int i = threadIdx.x; i < kImgRows * kPatch; i += 256) {
+    const int r = i / kPatch;
+    rows[r][i % kPatch] = r < nrows ? img[static_cast<size_t>(r0 + r) * kPatch + i % kPatch] : 0.f;
+  }
+  float w[kPatch];
+  const uint4* wr = reinterpret_cast<const uint4*>(W + static_cast<size_t>(col) * kPatch);
+#pragma unroll
+  for (int i = 0; i < kPatch / 8; ++i) {
+    const uint4 v = wr[i];
+    const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      w[8 * i + 2 * j] = __uint_as_float(q[j] << 16);
+      w[8 * i + 2 * j + 1] = __uint_as_float(q[j] & 0xFFFF0000u);
+    }
+  }
+  const float bias = bf16_bits_to_float(b[col]);
+  const float sc = 1.f + mod[col];  // image rows: sampled-t row, chunk s1
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int r = 0; r < nrows; ++r) {
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < kPatch; ++k) acc += rows[r][k] * w[k];
+    acc += bias;
+    const size_t idx = static_cast<size_t>(r0 + r) * kHidden + col;
+    x[idx] = acc;
+    xa[idx] = __float2bfloat16_rn(acc * sc);
+    const float s = warp_sum(acc * acc);
+    if (lane == 0) red[r][warp] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x < nrows) {
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += red[threadIdx.x][i];
+    ssp[static_cast<size_t>(r0 + threadIdx.x) * kSspParts + blockIdx.x] = s;
+  }
+}
+
+// ---------------------------------------------------------------- output head
+
+// vel[i] = (x[i] / rms(x[i])) . Wout^T + b, 4096 -> 64, with rms from the sum-of-squares
+// partials. Block: 16 rows x 64 outputs; K staged through shared memory 128 at a time.
+constexpr int kHeadRows = 16;
+constexpr int kHeadK = 128;
+__global__ void __launch_bounds__(256) head_kernel(const float* __restrict__ x, int N, const float* __restrict__ ssp,
+                                                   const uint16_t* __restrict__ W, const uint16_t* __restrict__ b,
+                                                   float* __restrict__ vel) {
+  __shared__ float wt[kHeadK][kPatch + 1];
+  __shared__ float xs[kHeadRows][kHeadK + 1];
+  const int r0 = blockIdx.x * kHeadRows;
+  const int i = threadIdx.x >> 4;   // row in block
+  const int oq = threadIdx.x & 15;  // outputs oq + 16 j
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+  for (int k0 = 0; k0 < kHidden; k0 += kHeadK) {
+    for (int e = threadIdx.x; e < kPatch * kHeadK; e += 256) {
+      const int o = e / kHeadK, k = e % kHeadK;
+      wt[k][o] = bf16_bits_to_float(W[static_cast<size_t>(o) * kHidden + k0 + k]);
+    }
+    for (int e = threadIdx.x; e < kHeadRows * kHeadK; e += 256) {
+      const int r = e / kHeadK, k = e % kHeadK;
+      xs[r][k] = (r0 + r) < N ? x[static_cast<size_t>(r0 + r) * kHidden + k0 + k] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int k = 0; k < kHeadK; ++k) {
+      const float xv = xs[i][k];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[j] += xv * wt[k][oq + 16 * j];
+    }
+    __syncthreads();
+  }
+  const int row = r0 + i;
+  if (row < N) {
+    const float4* p = reinterpret_cast<const float4*>(ssp + static_cast<size_t>(row) * kSspParts);
+    float s = 0.f;
+#pragma unroll
+    for (int q = 0; q < kSspParts / 4; ++q) {
+      const float4 v = p[q];
+      s += v.x;
+      s += v.y;
+      s += v.z;
+      s += v.w;
+    }
+    const float rinv = rsqrtf(s * (1.f / kHidden) + kEps);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int o = oq + 16 * j;
+      vel[static_cast<size_t>(row) * kPatch + o] = acc[j] * rinv + bf16_bits_to_float(b[o]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- RoPE tables
+
+// Value of axis table `axis` (width d = 16, 56, 56) at position pos, column k:
+// omega = fl32(theta^(-2k/d)) in double; angle = fl32(fl32(pos) * omega);
+// cos/sin evaluated in double and rounded once.
+__device__ __forceinline__ void rope_value(int axis, int k, int pos, double theta, float& c, float& s) {
+  const int d = axis == 0 ? 16 : 56;
+  const float w = static_cast<float>(pow(theta, -(2.0 * k) / d));
+  const float ang = __fmul_rn(static_cast<float>(pos), w);
+  c = static_cast<float>(cos(static_cast<double>(ang)));
+  s = static_cast<float>(sin(static_cast<double>(ang)));
+}
+
+__global__ void rope_axis_kernel(double theta, float* c0, float* s0, float* c1, float* s1, float* c2, float* s2) {
+  const int row = blockIdx.x;   // 0..9215
+  const int j = threadIdx.x;    // 0..63 -> axis columns 8 | 28 | 28
+  const int pos = row - 1024;
+  int axis, k, width;
+  float *cp, *sp;
+  if (j < 8) {
+    axis = 0; k = j; width = 8; cp = c0; sp = s0;
+  } else if (j < 36) {
+    axis = 1; k = j - 8; width = 28; cp = c1; sp = s1;
+  } else {
+    axis = 2; k = j - 36; width = 28; cp = c2; sp = s2;
+  }
+  float c, s;
+  rope_value(axis, k, pos, theta, c, s);
+  if (cp) cp[static_cast<size_t>(row) * width + k] = c;
+  if (sp) sp[static_cast<size_t>(row) * width + k] = s;
+}
+
+// Per-token rows: tokens [0, L) are text (i, i, i), [L, L + h*w) image.
+__global__ void rope_tokens_kernel(int L, int h, int w, double theta, float* tc, float* ts, float* ic, float* is) {
+  const int tok = blockIdx.x;
+  const int j = threadIdx.x;  // 0..63
+  int p0, p1, p2;
+  if (tok < L) {
+    p0 = p1 = p2 = tok;
+  } else {
+    const int n = tok - L;
+    const int y = n / w, xx = n % w;
+    p0 = L;
+    p1 = y - (h - h / 2);
+    p2 = xx - (w - w / 2);
+  }
+  int axis, k, pos;
+  if (j < 8) {
+    axis = 0; k = j; pos = p0;
+  } else if (j < 36) {
+    axis = 1; k = j - 8; pos = p1;
+  } else {
+    axis = 2; k = j - 36; pos = p2;
+  }
+  float c, s;
+  rope_value(axis, k, pos, theta, c, s);
+  float* cdst = tok < L ? tc : ic;
+  float* sdst = tok < L ? ts : is;
+  const size_t r = static_cast<size_t>(tok < L ? tok : tok - L);
+  if (cdst) cdst[r * kRopeCols + j] = c;
+  if (sdst) sdst[r * kRopeCols + j] = s;
+}
+
+// ---------------------------------------------------------------- sampler pieces
+
+__global__ void euler_kernel(float* __restrict__ x, const float* __restrict__ vel, long long n, float s_i,
+                             float s_next) {
+  const float dt = __fsub_rn(s_next, s_i);
+  const long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+  if (i + 3 < n) {
+    float4 a = *reinterpret_cast<float4*>(x + i);
+    const float4 v = *reinterpret_cast<const float4*>(vel + i);
+    a.x = __fadd_rn(a.x, __fmul_rn(dt, v.x));
+    a.y = __fadd_rn(a.y, __fmul_rn(dt, v.y));
+    a.z = __fadd_rn(a.z, __fmul_rn(dt, v.z));
+    a.w = __fadd_rn(a.w, __fmul_rn(dt, v.w));
+    *reinterpret_cast<float4*>(x + i) = a;
+  } else {
+    for (long long j = i; j < n; ++j) x[j] = __fadd_rn(x[j], __fmul_rn(dt, vel[j]));
+  }
+}
+
+// x[t, c] = z[c, t] for t < h*w, c < 64 (32x32 tiles through shared memory).
+__global__ void pack_noise_kernel(const float* __restrict__ z, int T, float* __restrict__ x) {
+  __shared__ float tile[32][33];
+  const int t0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int c = c0 + i, t = t0 + threadIdx.x;
+    tile[i][threadIdx.x] = t < T ? z[static_cast<size_t>(c) * T + t] : 0.f;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int t = t0 + i, c = c0 + threadIdx.x;
+    if (t < T) x[static_cast<size_t>(t) * kPatch + c] = tile[threadIdx.x][i];
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- launchers
+
+cudaError_t launch_timestep_embed(float t, float* e, cudaStream_t s) {
+  timestep_embed_kernel<<<1, 128, 0, s>>>(t, e);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemv2(const float* x, int in_dim, const uint16_t* W, const uint16_t* b, int out_dim, float* y,
+                         int silu_in, cudaStream_t s) {
+  const int per_block = 8 * kOutPerWarp;
+  const size_t smem = 2 * static_cast<size_t>(in_dim) * sizeof(float);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(gemv2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  gemv2_kernel<<<(out_dim + per_block - 1) / per_block, 256, smem, s>>>(x, in_dim, W, b, out_dim, y, silu_in);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_txt_prenorm(const float* txt, int L, const uint16_t* w, __nv_bfloat16* out, cudaStream_t s) {
+  if (L <= 0) return cudaSuccess;
+  txt_prenorm_kernel<<<L, 256, 0, s>>>(txt, w, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_block_prep(const float* x, int R, int n_text, const float* mod, __nv_bfloat16* xa, float* ssp,
+                              cudaStream_t s) {
+  if (R <= 0) return cudaSuccess;
+  block_prep_kernel<<<R, 256, 0, s>>>(x, n_text, mod, xa, ssp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_img_in(const float* img, int N, const uint16_t* W, const uint16_t* b, const float* mod, float* x,
+                          __nv_bfloat16* xa, float* ssp, cudaStream_t s) {
+  if (N <= 0) return cudaSuccess;
+  dim3 grid(kHidden / 256, (N + kImgRows - 1) / kImgRows);
+  img_in_kernel<<<grid, 256, 0, s>>>(img, N, W, b, mod, x, xa, ssp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_head(const float* x, int N, const float* ssp, const uint16_t* W, const uint16_t* b, float* vel,
+                        cudaStream_t s) {
+  if (N <= 0) return cudaSuccess;
+  head_kernel<<<(N + kHeadRows - 1) / kHeadRows, 256, 0, s>>>(x, N, ssp, W, b, vel);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_euler(float* x, const float* vel, long long n, float s_i, float s_next, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const long long threads = (n + 3) / 4;
+  euler_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(x, vel, n, s_i, s_next);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_axis(float theta, float* c0, float* s0, float* c1, float* s1, float* c2, float* s2,
+                             cudaStream_t s) {
+  rope_axis_kernel<<<9216, 64, 0, s>>>(static_cast<double>(theta), c0, s0, c1, s1, c2, s2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_tokens(int L, int h, int w, float theta, float* tc, float* ts, float* ic, float* is,
+                               cudaStream_t s) {
+  const int T = L + h * w;
+  if (T <= 0) return cudaSuccess;
+  rope_tokens_kernel<<<T, 64, 0, s>>>(L, h, w, static_cast<double>(theta), tc, ts, ic, is);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_noise(const float* z, int h, int w, float* x, cudaStream_t s) {
+  const int T = h * w;
+  if (T <= 0) return cudaSuccess;
+  dim3 grid((T + 31) / 32, kPatch / 32);
+  pack_noise_kernel<<<grid, dim3(32, 8), 0, s>>>(z, T, x);
+  return cudaGetLastError();
+}
+
+}  // namespace qi

@@ -1,0 +1,791 @@
+// C-ABI of the Qwen-Image-2.1 DiT step library: handle, weight store, pass
+// orchestration and the host-contract entry points (declared in include/qidit.h).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/qidit.h"
+#include "internal.h"
+
+using qi::kBN;
+using qi::kFfn;
+using qi::kHidden;
+using qi::kMod;
+using qi::kPatch;
+using qi::kRopeCols;
+using qi::kSspParts;
+using qi::kTdim;
+using bf16 = __nv_bfloat16;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+qi_status fail(qi_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+#define QI_CUDA(call)                                                                              \
+  do {                                                                                             \
+    cudaError_t e_ = (call);                                                                       \
+    if (e_ != cudaSuccess)                                                                         \
+      return fail(e_ == cudaErrorMemoryAllocation ? QI_ERR_OOM : QI_ERR_CUDA, "%s failed: %s (%s:%d)", \
+                  #call, cudaGetErrorString(e_), __FILE__, __LINE__);                              \
+  } while (0)
+
+#define QI_TRY(expr)                  \
+  do {                                \
+    qi_status s_ = (expr);            \
+    if (s_ != QI_OK) return s_;       \
+  } while (0)
+
+// ---------------------------------------------------------------- tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, cols] matrix; box = box_rows x 64 columns
+// (one 128-byte swizzle span), rows past `rows` read as zero.
+qi_status make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(QI_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (cols * 2) % 16 != 0)
+    return fail(QI_ERR_INVALID_ARG, "tensor map base or row pitch not 16-byte aligned");
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(QI_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return QI_OK;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+// ---------------------------------------------------------------- handle
+
+struct qi_dit {
+  int device = 0;
+  int blocks = 0;
+  int L_max = 0, N_max = 0, R_max = 0;
+  int num_sms = 0;
+  bool loaded_global = false;
+  std::vector<bool> loaded_block;
+
+  // weights (one allocation)
+  void* wmem = nullptr;
+  uint16_t *t_w1, *t_b1, *t_w2, *t_b2, *mod_w, *mod_b, *txt_norm_w, *txt_w, *txt_b, *img_w, *img_b, *out_w, *out_b;
+  struct Block {
+    uint16_t* wqkv;  // [3*4096, 4096]: Q rows, K rows, V rows
+    uint16_t* wo;    // [4096, 4096]
+    uint16_t* wgu;   // [2*12288, 4096]: per 128-row group j, gate rows then up rows
+    uint16_t* wd;    // [4096, 12288]
+    CUtensorMap m_qkv, m_o, m_gu, m_d;
+  };
+  std::vector<Block> blk;
+  CUtensorMap m_txt;
+
+  // activations (one allocation)
+  void* amem = nullptr;
+  float* x = nullptr;      // [R_max, 4096] fp32 residual stream
+  bf16* xa = nullptr;      // [R_max, 4096] bf16 modulated GEMM input
+  float* ssp = nullptr;    // [R_max, 16] sum-of-squares partials
+  bf16* q = nullptr;       // [R_max, 4096]
+  bf16* o = nullptr;       // [R_max, 4096] attention output
+  bf16* h = nullptr;       // [R_max, 12288] SwiGLU hidden
+  bf16* txt_a = nullptr;   // [L_max, 4096] text pre-norm output
+  float* temb_e = nullptr; // [2, 256]
+  float* temb_h = nullptr; // [2, 4096]
+  float* temb = nullptr;   // [2, 4096]
+  float* mod = nullptr;    // [2, 16384]: row 0 sampled t, row 1 t = 0
+  int* err = nullptr;      // device error word
+  bf16* kv = nullptr;      // [blocks][2][R_max][4096]
+  int cache_L = -1;        // L of the valid text K/V capture, -1 if none
+
+  // host-I/O staging (allocated on first use)
+  float *st_img = nullptr, *st_txt = nullptr, *st_tc = nullptr, *st_ts = nullptr, *st_ic = nullptr,
+        *st_is = nullptr, *st_vel = nullptr;
+
+  int trace_block[2] = {-1, -1};
+  float* trace_dst[2] = {nullptr, nullptr};
+
+  bool prof = false;
+  struct ProfEv {
+    int cls;
+    cudaEvent_t a, b;
+  };
+  std::vector<ProfEv> prof_ev;
+  size_t prof_used = 0;
+
+  bf16* k_of(int b) { return kv + static_cast<size_t>(b) * 2 * R_max * kHidden; }
+  bf16* v_of(int b) { return k_of(b) + static_cast<size_t>(R_max) * kHidden; }
+};
+
+namespace {
+
+enum PassMode { kJoint, kImage, kText };
+
+struct ProfScope {
+  qi_dit* d;
+  cudaStream_t s;
+  int cls;
+  qi_dit::ProfEv* ev = nullptr;
+  ProfScope(qi_dit* d_, cudaStream_t s_, int c) : d(d_), s(s_), cls(c) {
+    if (!d->prof) return;
+    if (d->prof_used == d->prof_ev.size()) {
+      qi_dit::ProfEv e{c, nullptr, nullptr};
+      cudaEventCreate(&e.a);
+      cudaEventCreate(&e.b);
+      d->prof_ev.push_back(e);
+    }
+    ev = &d->prof_ev[d->prof_used++];
+    ev->cls = c;
+    cudaEventRecord(ev->a, s);
+  }
+  ~ProfScope() {
+    if (ev) cudaEventRecord(ev->b, s);
+  }
+};
+
+qi_status check_device_word(qi_dit* d, cudaStream_t s) {
+  int h = 0;
+  QI_CUDA(cudaMemcpyAsync(&h, d->err, sizeof(int), cudaMemcpyDeviceToHost, s));
+  QI_CUDA(cudaStreamSynchronize(s));
+  if (h != 0) {
+    QI_CUDA(cudaMemsetAsync(d->err, 0, sizeof(int), s));
+    QI_CUDA(cudaStreamSynchronize(s));
+    return fail(QI_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired (device code %d)", h);
+  }
+  return QI_OK;
+}
+
+qi_status compute_mod(qi_dit* d, float t, cudaStream_t s) {
+  ProfScope ps(d, s, 5);
+  QI_CUDA(qi::launch_timestep_embed(t, d->temb_e, s));
+  QI_CUDA(qi::launch_gemv2(d->temb_e, kTdim, d->t_w1, d->t_b1, kHidden, d->temb_h, 0, s));
+  QI_CUDA(qi::launch_gemv2(d->temb_h, kHidden, d->t_w2, d->t_b2, kHidden, d->temb, 1, s));
+  QI_CUDA(qi::launch_gemv2(d->temb, kHidden, d->mod_w, d->mod_b, kMod, d->mod, 1, s));
+  return QI_OK;
+}
+
+// One block over `R` activation rows. n_text = rows that are text (they come
+// first); q_off = global index of activation row 0; Lk = keys image rows see.
+qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int Lk, const float* txt_cos,
+                    const float* txt_sin, const float* img_cos, const float* img_sin, cudaStream_t s) {
+  qi_dit::Block& B = d->blk[b];
+  CUtensorMap m_xa, m_o, m_h;
+  QI_TRY(make_map(&m_xa, d->xa, R, kHidden, 128));
+  QI_TRY(make_map(&m_o, d->o, R, kHidden, 128));
+  QI_TRY(make_map(&m_h, d->h, R, kFfn, 128));
+
+  qi::GemmParams p{};
+  p.M = R;
+  p.n_text = n_text;
+  p.mod = d->mod;
+  p.err = d->err;
+
+  // QKV + 1/rms + RoPE -> Q and this block's K/V store
+  {
+    ProfScope ps(d, s, 0);
+    qi::GemmParams g = p;
+    g.N = 3 * kHidden;
+    g.K = kHidden;
+    g.ssp_in = d->ssp;
+    g.q = d->q;
+    g.k = d->k_of(b);
+    g.v = d->v_of(b);
+    g.kv_row_off = q_off;
+    g.txt_cos = txt_cos;
+    g.txt_sin = txt_sin;
+    g.img_cos = img_cos;
+    g.img_sin = img_sin;
+    QI_CUDA(qi::launch_gemm(qi::kEpiQkv, m_xa, B.m_qkv, g, d->num_sms, s));
+  }
+  // block-causal attention
+  {
+    ProfScope ps(d, s, 1);
+    qi::AttnParams a{};
+    a.q = d->q;
+    a.k = d->k_of(b);
+    a.v = d->v_of(b);
+    a.o = d->o;
+    a.Rq = R;
+    a.q_off = q_off;
+    a.L = L;
+    a.Lk = Lk;
+    QI_CUDA(qi::launch_attention(a, s));
+  }
+  // out-projection: x += g1 * (o Wo^T); xa = bf16(x (1 + s2))
+  {
+    ProfScope ps(d, s, 2);
+    qi::GemmParams g = p;
+    g.N = kHidden;
+    g.K = kHidden;
+    g.x = d->x;
+    g.xa = d->xa;
+    g.ssp_out = d->ssp;
+    g.resid_set = 0;
+    g.gate_chunk = 1;
+    g.scale_chunk = 2;
+    QI_CUDA(qi::launch_gemm(qi::kEpiResid, m_o, B.m_o, g, d->num_sms, s));
+  }
+  // gate/up + SwiGLU
+  {
+    ProfScope ps(d, s, 3);
+    qi::GemmParams g = p;
+    g.N = 2 * kFfn;
+    g.K = kHidden;
+    g.ssp_in = d->ssp;
+    g.h = d->h;
+    QI_CUDA(qi::launch_gemm(qi::kEpiSwiglu, m_xa, B.m_gu, g, d->num_sms, s));
+  }
+  // down: x += g2 * (h Wd^T); xa = bf16(x (1 + s1)) for the next block
+  {
+    ProfScope ps(d, s, 4);
+    qi::GemmParams g = p;
+    g.N = kHidden;
+    g.K = kFfn;
+    g.x = d->x;
+    g.xa = d->xa;
+    g.ssp_out = d->ssp;
+    g.resid_set = 0;
+    g.gate_chunk = 3;
+    g.scale_chunk = 0;
+    QI_CUDA(qi::launch_gemm(qi::kEpiResid, m_h, B.m_d, g, d->num_sms, s));
+  }
+  return QI_OK;
+}
+
+qi_status trace_copy(qi_dit* d, int at_block, int R, cudaStream_t s) {
+  for (int i = 0; i < 2; ++i)
+    if (d->trace_dst[i] && d->trace_block[i] == at_block)
+      QI_CUDA(cudaMemcpyAsync(d->trace_dst[i], d->x, static_cast<size_t>(R) * kHidden * sizeof(float),
+                              cudaMemcpyDeviceToDevice, s));
+  return QI_OK;
+}
+
+// The whole pass. Joint: rows [text L | image N]; image: rows [image N] with the
+// stored text K/V; text: rows [text L], no head.
+qi_status run_pass(qi_dit* d, PassMode mode, const float* img, int N, const float* txt, int L, float t,
+                   const float* tc, const float* ts, const float* ic, const float* is, float* vel,
+                   cudaStream_t s) {
+  const int n_text = mode == kImage ? 0 : L;
+  const int n_img = mode == kText ? 0 : N;
+  const int R = n_text + n_img;
+  const int q_off = mode == kImage ? L : 0;
+  const int Lk = mode == kText ? L : L + N;
+
+  QI_TRY(compute_mod(d, t, s));
+  {
+    ProfScope ps(d, s, 5);
+    if (n_text > 0) {
+      QI_CUDA(qi::launch_txt_prenorm(txt, L, d->txt_norm_w, d->txt_a, s));
+    }
+    if (n_img > 0) {
+      const size_t off = static_cast<size_t>(n_text);
+      QI_CUDA(qi::launch_img_in(img, N, d->img_w, d->img_b, d->mod, d->x + off * kHidden, d->xa + off * kHidden,
+                                d->ssp + off * kSspParts, s));
+    }
+  }
+  if (n_text > 0) {
+    ProfScope ps(d, s, 5);
+    CUtensorMap m_a;
+    QI_TRY(make_map(&m_a, d->txt_a, L, kHidden, 128));
+    qi::GemmParams g{};
+    g.M = L;
+    g.N = kHidden;
+    g.K = kHidden;
+    g.n_text = L;
+    g.mod = d->mod;
+    g.err = d->err;
+    g.x = d->x;
+    g.xa = d->xa;
+    g.ssp_out = d->ssp;
+    g.bias = d->txt_b;
+    g.resid_set = 1;
+    g.gate_chunk = 1;
+    g.scale_chunk = 0;
+    QI_CUDA(qi::launch_gemm(qi::kEpiResid, m_a, d->m_txt, g, d->num_sms, s));
+  }
+  for (int b = 0; b < d->blocks; ++b) {
+    QI_TRY(trace_copy(d, b, R, s));
+    QI_TRY(run_block(d, b, R, n_text, q_off, L, Lk, tc, ts, ic, is, s));
+  }
+  QI_TRY(trace_copy(d, d->blocks, R, s));
+  if (n_img > 0) {
+    ProfScope ps(d, s, 5);
+    const size_t off = static_cast<size_t>(n_text);
+    QI_CUDA(qi::launch_head(d->x + off * kHidden, N, d->ssp + off * kSspParts, d->out_w, d->out_b, vel, s));
+  }
+  return QI_OK;
+}
+
+bool all_loaded(const qi_dit* d) {
+  if (!d->loaded_global) return false;
+  for (bool b : d->loaded_block)
+    if (!b) return false;
+  return true;
+}
+
+}  // namespace
+
+// ================================================================ C ABI
+
+extern "C" {
+
+const char* qi_last_error(void) { return g_last_error.c_str(); }
+
+size_t qi_kv_cache_bytes(int blocks, int L) {
+  if (blocks <= 0 || L <= 0) return 0;
+  return static_cast<size_t>(2) * blocks * L * kHidden * 2;
+}
+
+qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out) {
+  if (!cfg || !out) return fail(QI_ERR_INVALID_ARG, "qi_dit_create: NULL argument");
+  *out = nullptr;
+  if (cfg->blocks < 1 || cfg->blocks > QI_BLOCKS || cfg->L_max < QI_L_MIN || cfg->L_max > QI_L_MAX ||
+      cfg->N_max < QI_N_MIN || cfg->N_max > QI_N_MAX)
+    return fail(QI_ERR_SHAPE, "qi_dit_create: blocks %d L_max %d N_max %d out of range", cfg->blocks, cfg->L_max,
+                cfg->N_max);
+  QI_CUDA(cudaSetDevice(device));
+  qi_dit* d = new qi_dit();
+  d->device = device;
+  d->blocks = cfg->blocks;
+  d->L_max = cfg->L_max;
+  d->N_max = cfg->N_max;
+  d->R_max = cfg->L_max + cfg->N_max;
+  d->loaded_block.assign(cfg->blocks, false);
+  cudaDeviceGetAttribute(&d->num_sms, cudaDevAttrMultiProcessorCount, device);
+
+  // ---- weights
+  const size_t A = 256;
+  struct Seg {
+    uint16_t** p;
+    size_t n;
+  };
+  std::vector<Seg> segs = {
+      {&d->t_w1, (size_t)kHidden * kTdim}, {&d->t_b1, (size_t)kHidden},
+      {&d->t_w2, (size_t)kHidden * kHidden}, {&d->t_b2, (size_t)kHidden},
+      {&d->mod_w, (size_t)kMod * kHidden}, {&d->mod_b, (size_t)kMod},
+      {&d->txt_norm_w, (size_t)kHidden}, {&d->txt_w, (size_t)kHidden * kHidden},
+      {&d->txt_b, (size_t)kHidden}, {&d->img_w, (size_t)kHidden * kPatch},
+      {&d->img_b, (size_t)kHidden}, {&d->out_w, (size_t)kPatch * kHidden},
+      {&d->out_b, (size_t)kPatch},
+  };
+  d->blk.resize(cfg->blocks);
+  for (auto& b : d->blk) {
+    segs.push_back({&b.wqkv, (size_t)3 * kHidden * kHidden});
+    segs.push_back({&b.wo, (size_t)kHidden * kHidden});
+    segs.push_back({&b.wgu, (size_t)2 * kFfn * kHidden});
+    segs.push_back({&b.wd, (size_t)kHidden * kFfn});
+  }
+  size_t wbytes = 0;
+  for (auto& s : segs) wbytes += align_up(s.n * 2, A);
+  cudaError_t e = cudaMalloc(&d->wmem, wbytes);
+  if (e != cudaSuccess) {
+    delete d;
+    return fail(QI_ERR_OOM, "qi_dit_create: weight store of %zu bytes: %s", wbytes, cudaGetErrorString(e));
+  }
+  {
+    char* p = static_cast<char*>(d->wmem);
+    for (auto& s : segs) {
+      *s.p = reinterpret_cast<uint16_t*>(p);
+      p += align_up(s.n * 2, A);
+    }
+  }
+
+  // ---- activations and K/V store
+  const size_t R = d->R_max;
+  struct ASeg {
+    void** p;
+    size_t bytes;
+  };
+  std::vector<ASeg> asegs = {
+      {(void**)&d->x, R * kHidden * 4},   {(void**)&d->xa, R * kHidden * 2},
+      {(void**)&d->ssp, R * kSspParts * 4}, {(void**)&d->q, R * kHidden * 2},
+      {(void**)&d->o, R * kHidden * 2},   {(void**)&d->h, R * kFfn * 2},
+      {(void**)&d->txt_a, (size_t)d->L_max * kHidden * 2}, {(void**)&d->temb_e, 2 * kTdim * 4},
+      {(void**)&d->temb_h, 2 * kHidden * 4}, {(void**)&d->temb, 2 * kHidden * 4},
+      {(void**)&d->mod, 2 * (size_t)kMod * 4}, {(void**)&d->err, 256},
+      {(void**)&d->kv, (size_t)cfg->blocks * 2 * R * kHidden * 2},
+  };
+  size_t abytes = 0;
+  for (auto& s : asegs) abytes += align_up(s.bytes, 1024);
+  e = cudaMalloc(&d->amem, abytes);
+  if (e != cudaSuccess) {
+    cudaFree(d->wmem);
+    delete d;
+    return fail(QI_ERR_OOM, "qi_dit_create: activations of %zu bytes: %s", abytes, cudaGetErrorString(e));
+  }
+  {
+    char* p = static_cast<char*>(d->amem);
+    for (auto& s : asegs) {
+      *s.p = p;
+      p += align_up(s.bytes, 1024);
+    }
+  }
+  cudaMemset(d->amem, 0, abytes);
+
+  // ---- weight tensor maps (B operands: 256-row boxes)
+  qi_status st = make_map(&d->m_txt, d->txt_w, kHidden, kHidden, 256);
+  for (int b = 0; st == QI_OK && b < cfg->blocks; ++b) {
+    auto& B = d->blk[b];
+    st = make_map(&B.m_qkv, B.wqkv, 3 * kHidden, kHidden, 256);
+    if (st == QI_OK) st = make_map(&B.m_o, B.wo, kHidden, kHidden, 256);
+    if (st == QI_OK) st = make_map(&B.m_gu, B.wgu, 2 * kFfn, kHidden, 256);
+    if (st == QI_OK) st = make_map(&B.m_d, B.wd, kHidden, kFfn, 256);
+  }
+  if (st != QI_OK) {
+    cudaFree(d->amem);
+    cudaFree(d->wmem);
+    delete d;
+    return st;
+  }
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(d->amem);
+    cudaFree(d->wmem);
+    delete d;
+    return fail(QI_ERR_CUDA, "qi_dit_create: %s", cudaGetErrorString(e));
+  }
+  *out = d;
+  return QI_OK;
+}
+
+qi_status qi_dit_destroy(qi_dit* d) {
+  if (!d) return QI_OK;
+  cudaSetDevice(d->device);
+  cudaDeviceSynchronize();
+  for (auto& e : d->prof_ev) {
+    cudaEventDestroy(e.a);
+    cudaEventDestroy(e.b);
+  }
+  float* st[] = {d->st_img, d->st_txt, d->st_tc, d->st_ts, d->st_ic, d->st_is, d->st_vel};
+  for (float* p : st)
+    if (p) cudaFree(p);
+  cudaFree(d->amem);
+  cudaFree(d->wmem);
+  delete d;
+  return QI_OK;
+}
+
+qi_status qi_dit_load_global(qi_dit* d, const qi_global_weights* w, int src_on_device, qi_stream_t stream) {
+  if (!d || !w) return fail(QI_ERR_INVALID_ARG, "qi_dit_load_global: NULL argument");
+  const void* src[] = {w->t_w1, w->t_b1, w->t_w2, w->t_b2, w->mod_w, w->mod_b, w->txt_norm_w,
+                       w->txt_w, w->txt_b, w->img_w, w->img_b, w->out_w, w->out_b};
+  uint16_t* dst[] = {d->t_w1, d->t_b1, d->t_w2, d->t_b2, d->mod_w, d->mod_b, d->txt_norm_w,
+                     d->txt_w, d->txt_b, d->img_w, d->img_b, d->out_w, d->out_b};
+  const size_t n[] = {(size_t)kHidden * kTdim, kHidden, (size_t)kHidden * kHidden, kHidden,
+                      (size_t)kMod * kHidden, kMod, kHidden, (size_t)kHidden * kHidden, kHidden,
+                      (size_t)kHidden * kPatch, kHidden, (size_t)kPatch * kHidden, kPatch};
+  for (int i = 0; i < 13; ++i)
+    if (!src[i]) return fail(QI_ERR_INVALID_ARG, "qi_dit_load_global: tensor %d is NULL", i);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  QI_CUDA(cudaSetDevice(d->device));
+  const cudaMemcpyKind kind = src_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+  for (int i = 0; i < 13; ++i) QI_CUDA(cudaMemcpyAsync(dst[i], src[i], n[i] * 2, kind, s));
+  QI_CUDA(cudaStreamSynchronize(s));
+  d->loaded_global = true;
+  return QI_OK;
+}
+
+qi_status qi_dit_load_block(qi_dit* d, int block, const qi_block_weights* w, int src_on_device,
+                            qi_stream_t stream) {
+  if (!d || !w) return fail(QI_ERR_INVALID_ARG, "qi_dit_load_block: NULL argument");
+  if (block < 0 || block >= d->blocks) return fail(QI_ERR_INVALID_ARG, "qi_dit_load_block: block %d", block);
+  if (!w->wq || !w->wk || !w->wv || !w->wo || !w->wg || !w->wu || !w->wd)
+    return fail(QI_ERR_INVALID_ARG, "qi_dit_load_block: a tensor is NULL");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  QI_CUDA(cudaSetDevice(d->device));
+  const cudaMemcpyKind kind = src_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+  auto& B = d->blk[block];
+  const size_t sq = (size_t)kHidden * kHidden;
+  QI_CUDA(cudaMemcpyAsync(B.wqkv, w->wq, sq * 2, kind, s));
+  QI_CUDA(cudaMemcpyAsync(B.wqkv + sq, w->wk, sq * 2, kind, s));
+  QI_CUDA(cudaMemcpyAsync(B.wqkv + 2 * sq, w->wv, sq * 2, kind, s));
+  QI_CUDA(cudaMemcpyAsync(B.wo, w->wo, sq * 2, kind, s));
+  // gate/up interleave: 128-row groups, gate group j then up group j
+  const size_t grp = (size_t)(kBN / 2) * kHidden * 2;  // bytes per 128-row group
+  QI_CUDA(cudaMemcpy2DAsync(B.wgu, 2 * grp, w->wg, grp, grp, kFfn / (kBN / 2), kind, s));
+  QI_CUDA(cudaMemcpy2DAsync(reinterpret_cast<char*>(B.wgu) + grp, 2 * grp, w->wu, grp, grp, kFfn / (kBN / 2), kind,
+                            s));
+  QI_CUDA(cudaMemcpyAsync(B.wd, w->wd, (size_t)kHidden * kFfn * 2, kind, s));
+  QI_CUDA(cudaStreamSynchronize(s));
+  d->loaded_block[block] = true;
+  return QI_OK;
+}
+
+qi_status qi_rope_axis_tables(float theta, float* cos0, float* sin0, float* cos1, float* sin1, float* cos2,
+                              float* sin2, qi_stream_t stream) {
+  if (!(theta > 1.f)) return fail(QI_ERR_INVALID_ARG, "qi_rope_axis_tables: theta %g", theta);
+  QI_CUDA(qi::launch_rope_axis(theta, cos0, sin0, cos1, sin1, cos2, sin2, reinterpret_cast<cudaStream_t>(stream)));
+  return QI_OK;
+}
+
+qi_status qi_rope_tables(int L, int h, int w, float theta, float* txt_cos, float* txt_sin, float* img_cos,
+                         float* img_sin, qi_stream_t stream) {
+  if (L < QI_L_MIN || L > QI_L_MAX || h < 1 || w < 1 || (long long)h * w > QI_N_MAX)
+    return fail(QI_ERR_SHAPE, "qi_rope_tables: L %d h %d w %d out of range", L, h, w);
+  // every position must fall inside the table range -1024..8191
+  if (h - h / 2 > 1024 || w - w / 2 > 1024 || L > 8191)
+    return fail(QI_ERR_SHAPE, "qi_rope_tables: positions leave the table range");
+  if (!(theta > 1.f)) return fail(QI_ERR_INVALID_ARG, "qi_rope_tables: theta %g", theta);
+  QI_CUDA(qi::launch_rope_tokens(L, h, w, theta, txt_cos, txt_sin, img_cos, img_sin,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+  return QI_OK;
+}
+
+qi_status qi_flow_sigmas(int steps, int N, const qi_sched_params* p, float* sigmas, float* timesteps) {
+  if (!sigmas || !timesteps) return fail(QI_ERR_INVALID_ARG, "qi_flow_sigmas: NULL output");
+  // one step makes the terminal stretch 0/0 (its only sigma is 1), so at least two
+  if (steps < 2 || N < 1) return fail(QI_ERR_SHAPE, "qi_flow_sigmas: steps %d (>= 2) N %d", steps, N);
+  const qi_sched_params def = {0.5, 0.9, 256, 8192, 0.02, 1000};
+  const qi_sched_params& c = p ? *p : def;
+  if (c.max_seq == c.base_seq || c.shift_terminal >= 1.0)
+    return fail(QI_ERR_INVALID_ARG, "qi_flow_sigmas: bad scheduler constants");
+  // linspace(1, 1/steps, steps): start + i * step, last entry exactly the end point
+  std::vector<double> s(steps);
+  const double start = 1.0, stop = 1.0 / steps;
+  if (steps == 1) {
+    s[0] = start;
+  } else {
+    const double step = (stop - start) / (steps - 1);
+    for (int i = 0; i < steps; ++i) s[i] = i * step + start;
+    s[steps - 1] = stop;
+  }
+  const double m = (c.max_shift - c.base_shift) / (c.max_seq - c.base_seq);
+  const double b = c.base_shift - m * c.base_seq;
+  const double mu = N * m + b;
+  const double e = std::exp(mu);
+  for (int i = 0; i < steps; ++i) s[i] = e / (e + (1.0 / s[i] - 1.0));
+  const double scale = (1.0 - s[steps - 1]) / (1.0 - c.shift_terminal);
+  for (int i = 0; i < steps; ++i) s[i] = 1.0 - (1.0 - s[i]) / scale;
+  for (int i = 0; i < steps; ++i) {
+    timesteps[i] = static_cast<float>(s[i] * c.train_steps);
+    sigmas[i] = static_cast<float>(s[i]);
+  }
+  sigmas[steps] = 0.f;
+  return QI_OK;
+}
+
+qi_status qi_pack_noise(const float* z, int h, int w, float* x, qi_stream_t stream) {
+  if (!z || !x) return fail(QI_ERR_INVALID_ARG, "qi_pack_noise: NULL argument");
+  if (h < 1 || w < 1 || (long long)h * w > QI_N_MAX) return fail(QI_ERR_SHAPE, "qi_pack_noise: h %d w %d", h, w);
+  QI_CUDA(qi::launch_pack_noise(z, h, w, x, reinterpret_cast<cudaStream_t>(stream)));
+  return QI_OK;
+}
+
+qi_status qi_euler_update(float* x, const float* vel, int N, float sigma_i, float sigma_next, qi_stream_t stream) {
+  if (!x || !vel) return fail(QI_ERR_INVALID_ARG, "qi_euler_update: NULL argument");
+  if (N < 0) return fail(QI_ERR_SHAPE, "qi_euler_update: N %d", N);
+  QI_CUDA(qi::launch_euler(x, vel, static_cast<long long>(N) * kPatch, sigma_i, sigma_next,
+                           reinterpret_cast<cudaStream_t>(stream)));
+  return QI_OK;
+}
+
+qi_status qi_dit_step(qi_dit* d, const float* img_tokens, int N, const float* txt_feats, int L, float timestep,
+                      const float* txt_cos, const float* txt_sin, const float* img_cos, const float* img_sin,
+                      float* vel, unsigned flags, qi_stream_t stream) {
+  if (!d) return fail(QI_ERR_INVALID_ARG, "qi_dit_step: NULL handle");
+  if (flags & ~(QI_STEP_USE_CACHE | QI_STEP_HOST_IO)) return fail(QI_ERR_INVALID_ARG, "qi_dit_step: flags %u", flags);
+  const bool use_cache = flags & QI_STEP_USE_CACHE;
+  const bool host_io = flags & QI_STEP_HOST_IO;
+  if (N < QI_N_MIN || N > d->N_max || L < QI_L_MIN || L > d->L_max)
+    return fail(QI_ERR_SHAPE, "qi_dit_step: N %d (max %d) L %d (max %d)", N, d->N_max, L, d->L_max);
+  if (!img_tokens || !img_cos || !img_sin || !vel) return fail(QI_ERR_INVALID_ARG, "qi_dit_step: NULL image tensor");
+  if (!use_cache && (!txt_feats || !txt_cos || !txt_sin))
+    return fail(QI_ERR_INVALID_ARG, "qi_dit_step: joint pass needs txt_feats and txt_cos/txt_sin");
+  if (use_cache && d->cache_L != L)
+    return fail(QI_ERR_STATE, "qi_dit_step: USE_CACHE but the text K/V capture is for L=%d, not %d", d->cache_L, L);
+  if (!all_loaded(d)) return fail(QI_ERR_STATE, "qi_dit_step: weights not loaded");
+  if (!std::isfinite(timestep)) return fail(QI_ERR_INVALID_ARG, "qi_dit_step: timestep not finite");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  QI_CUDA(cudaSetDevice(d->device));
+
+  if (host_io) {
+    if (!d->st_img) {
+      QI_CUDA(cudaMalloc(&d->st_img, (size_t)d->N_max * kPatch * 4));
+      QI_CUDA(cudaMalloc(&d->st_vel, (size_t)d->N_max * kPatch * 4));
+      QI_CUDA(cudaMalloc(&d->st_ic, (size_t)d->N_max * kRopeCols * 4));
+      QI_CUDA(cudaMalloc(&d->st_is, (size_t)d->N_max * kRopeCols * 4));
+      QI_CUDA(cudaMalloc(&d->st_txt, (size_t)d->L_max * kHidden * 4));
+      QI_CUDA(cudaMalloc(&d->st_tc, (size_t)d->L_max * kRopeCols * 4));
+      QI_CUDA(cudaMalloc(&d->st_ts, (size_t)d->L_max * kRopeCols * 4));
+    }
+    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
+    QI_CUDA(cudaMemcpyAsync(d->st_img, img_tokens, (size_t)N * kPatch * 4, h2d, s));
+    QI_CUDA(cudaMemcpyAsync(d->st_ic, img_cos, (size_t)N * kRopeCols * 4, h2d, s));
+    QI_CUDA(cudaMemcpyAsync(d->st_is, img_sin, (size_t)N * kRopeCols * 4, h2d, s));
+    if (!use_cache) {
+      QI_CUDA(cudaMemcpyAsync(d->st_txt, txt_feats, (size_t)L * kHidden * 4, h2d, s));
+      QI_CUDA(cudaMemcpyAsync(d->st_tc, txt_cos, (size_t)L * kRopeCols * 4, h2d, s));
+      QI_CUDA(cudaMemcpyAsync(d->st_ts, txt_sin, (size_t)L * kRopeCols * 4, h2d, s));
+    }
+    QI_TRY(run_pass(d, use_cache ? kImage : kJoint, d->st_img, N, d->st_txt, L, timestep, d->st_tc, d->st_ts,
+                    d->st_ic, d->st_is, d->st_vel, s));
+    QI_CUDA(cudaMemcpyAsync(vel, d->st_vel, (size_t)N * kPatch * 4, cudaMemcpyDeviceToHost, s));
+    if (!use_cache) d->cache_L = L;
+    return check_device_word(d, s);
+  }
+  QI_TRY(run_pass(d, use_cache ? kImage : kJoint, img_tokens, N, txt_feats, L, timestep, txt_cos, txt_sin, img_cos,
+                  img_sin, vel, s));
+  if (!use_cache) d->cache_L = L;
+  return QI_OK;
+}
+
+qi_status qi_text_kv_capture(qi_dit* d, const float* txt_feats, int L, const float* txt_cos, const float* txt_sin,
+                             qi_stream_t stream) {
+  if (!d || !txt_feats || !txt_cos || !txt_sin) return fail(QI_ERR_INVALID_ARG, "qi_text_kv_capture: NULL argument");
+  if (L < QI_L_MIN || L > d->L_max) return fail(QI_ERR_SHAPE, "qi_text_kv_capture: L %d (max %d)", L, d->L_max);
+  if (!all_loaded(d)) return fail(QI_ERR_STATE, "qi_text_kv_capture: weights not loaded");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  QI_CUDA(cudaSetDevice(d->device));
+  QI_TRY(run_pass(d, kText, nullptr, 0, txt_feats, L, 0.f, txt_cos, txt_sin, nullptr, nullptr, nullptr, s));
+  d->cache_L = L;
+  return QI_OK;
+}
+
+qi_status qi_dit_check(qi_dit* d, qi_stream_t stream) {
+  if (!d) return fail(QI_ERR_INVALID_ARG, "qi_dit_check: NULL handle");
+  QI_CUDA(cudaSetDevice(d->device));
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(QI_ERR_CUDA, "qi_dit_check: %s", cudaGetErrorString(e));
+  return check_device_word(d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qi_status qi_dit_block_forward(qi_dit* d, int block, float* hidden, int L, int N, float t_img, const float* cos,
+                               const float* sin, qi_stream_t stream) {
+  if (!d || !hidden || !cos || !sin) return fail(QI_ERR_INVALID_ARG, "qi_dit_block_forward: NULL argument");
+  if (block < 0 || block >= d->blocks) return fail(QI_ERR_INVALID_ARG, "qi_dit_block_forward: block %d", block);
+  if (L < 0 || N < 0 || L + N < 1 || L > d->L_max || N > d->N_max)
+    return fail(QI_ERR_SHAPE, "qi_dit_block_forward: L %d N %d", L, N);
+  if (!d->loaded_global || !d->loaded_block[block]) return fail(QI_ERR_STATE, "qi_dit_block_forward: not loaded");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  QI_CUDA(cudaSetDevice(d->device));
+  const int R = L + N;
+  QI_CUDA(cudaMemcpyAsync(d->x, hidden, (size_t)R * kHidden * 4, cudaMemcpyDeviceToDevice, s));
+  QI_TRY(compute_mod(d, t_img, s));
+  QI_CUDA(qi::launch_block_prep(d->x, R, L, d->mod, d->xa, d->ssp, s));
+  QI_TRY(run_block(d, block, R, L, 0, L, R, cos, sin, cos + (size_t)L * kRopeCols, sin + (size_t)L * kRopeCols, s));
+  QI_CUDA(cudaMemcpyAsync(hidden, d->x, (size_t)R * kHidden * 4, cudaMemcpyDeviceToDevice, s));
+  return QI_OK;
+}
+
+qi_status qi_dit_read_kv(qi_dit* d, int block, int row0, int rows, uint16_t* k_out, uint16_t* v_out,
+                         qi_stream_t stream) {
+  if (!d || !k_out || !v_out) return fail(QI_ERR_INVALID_ARG, "qi_dit_read_kv: NULL argument");
+  if (block < 0 || block >= d->blocks) return fail(QI_ERR_INVALID_ARG, "qi_dit_read_kv: block %d", block);
+  if (row0 < 0 || rows < 0 || row0 + rows > d->R_max)
+    return fail(QI_ERR_SHAPE, "qi_dit_read_kv: rows [%d, %d) past %d", row0, row0 + rows, d->R_max);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  QI_CUDA(cudaSetDevice(d->device));
+  const size_t bytes = (size_t)rows * kHidden * 2;
+  QI_CUDA(cudaMemcpyAsync(k_out, d->k_of(block) + (size_t)row0 * kHidden, bytes, cudaMemcpyDeviceToDevice, s));
+  QI_CUDA(cudaMemcpyAsync(v_out, d->v_of(block) + (size_t)row0 * kHidden, bytes, cudaMemcpyDeviceToDevice, s));
+  return QI_OK;
+}
+
+qi_status qi_gemm_bf16(qi_dit* d, const uint16_t* A, const uint16_t* B, float* D, int M, int N, int K,
+                       qi_stream_t stream) {
+  if (!d || !A || !B || !D) return fail(QI_ERR_INVALID_ARG, "qi_gemm_bf16: NULL argument");
+  if (M < 1 || N < kBN || N % kBN != 0 || K < qi::kBK || K % qi::kBK != 0)
+    return fail(QI_ERR_SHAPE, "qi_gemm_bf16: M %d N %d K %d", M, N, K);
+  CUtensorMap ma, mb;
+  QI_TRY(make_map(&ma, A, M, K, 128));
+  QI_TRY(make_map(&mb, B, N, K, 256));
+  qi::GemmParams g{};
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.d = D;
+  g.err = d->err;
+  QI_CUDA(cudaSetDevice(d->device));
+  QI_CUDA(qi::launch_gemm(qi::kEpiF32, ma, mb, g, d->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+  return QI_OK;
+}
+
+qi_status qi_attention_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, int Rq, int q_off,
+                            int L, int Lk, qi_stream_t stream) {
+  if (!q || !k || !v || !o) return fail(QI_ERR_INVALID_ARG, "qi_attention_bf16: NULL argument");
+  if (Rq < 0 || q_off < 0 || L < 0 || Lk < 1 || L > Lk || q_off + Rq > Lk)
+    return fail(QI_ERR_SHAPE, "qi_attention_bf16: Rq %d q_off %d L %d Lk %d", Rq, q_off, L, Lk);
+  qi::AttnParams a{};
+  a.q = reinterpret_cast<const bf16*>(q);
+  a.k = reinterpret_cast<const bf16*>(k);
+  a.v = reinterpret_cast<const bf16*>(v);
+  a.o = reinterpret_cast<bf16*>(o);
+  a.Rq = Rq;
+  a.q_off = q_off;
+  a.L = L;
+  a.Lk = Lk;
+  QI_CUDA(qi::launch_attention(a, reinterpret_cast<cudaStream_t>(stream)));
+  return QI_OK;
+}
+
+qi_status qi_dit_set_trace(qi_dit* d, int slot, int block, float* dst) {
+  if (!d || slot < 0 || slot > 1) return fail(QI_ERR_INVALID_ARG, "qi_dit_set_trace: bad handle or slot");
+  if (dst && (block < 0 || block > d->blocks)) return fail(QI_ERR_INVALID_ARG, "qi_dit_set_trace: block %d", block);
+  d->trace_block[slot] = dst ? block : -1;
+  d->trace_dst[slot] = dst;
+  return QI_OK;
+}
+
+qi_status qi_dit_profile(qi_dit* d, int enable) {
+  if (!d) return fail(QI_ERR_INVALID_ARG, "qi_dit_profile: NULL handle");
+  d->prof = enable != 0;
+  d->prof_used = 0;
+  return QI_OK;
+}
+
+qi_status qi_dit_profile_read(qi_dit* d, double* ms, long long* launches) {
+  if (!d || !ms || !launches) return fail(QI_ERR_INVALID_ARG, "qi_dit_profile_read: NULL argument");
+  for (int c = 0; c < QI_PROF_CLASSES; ++c) {
+    ms[c] = 0.0;
+    launches[c] = 0;
+  }
+  QI_CUDA(cudaSetDevice(d->device));
+  for (size_t i = 0; i < d->prof_used; ++i) {
+    auto& e = d->prof_ev[i];
+    QI_CUDA(cudaEventSynchronize(e.b));
+    float t = 0.f;
+    QI_CUDA(cudaEventElapsedTime(&t, e.a, e.b));
+    ms[e.cls] += t;
+    launches[e.cls] += 1;
+  }
+  d->prof_used = 0;
+  return QI_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,277 @@
+/*
+ * qidit.h - C ABI of the GB300 (sm_103a) Qwen-Image-2.1 DiT step library.
+ *
+ * The library runs the forward pass of the 7B single-stream DiT denoiser of
+ * Qwen-Image-2.1 once per FlowMatch Euler step, plus the host-contract pieces
+ * around it (RoPE tables, sigma schedule, noise packing, Euler update).
+ *
+ * Sources (page titles, sections):
+ *   [ARCH]  "Qwen-Image-2.1 Core AI port" (coreai-model-zoo knowledge page),
+ *           architecture table, DiT row: 32 single-stream blocks, one shared
+ *           modulation Linear 4096->16384 with rows for the sampled t and t = 0,
+ *           ZeroCenterRMSNorm text projection, SwiGLU x3, 3-axis interleaved
+ *           RoPE (16/56/56), block-causal attention; graph I/O shapes.
+ *   [HOST]  "Host contract - RGBA-Image-2.1", section 1 (graph I/O, fp32 at the
+ *           boundary), section 4 (sequence layout, positions, RoPE tables),
+ *           section 5 (noise packing), section 6 (sampler).
+ *   [REUSE] "Qwen-Image-2.1 on MLX, faster and exact", section "Text K/V reuse":
+ *           text rows use the t = 0 modulation row and causal attention over
+ *           text only, so their K/V are constant over a whole run.
+ *
+ * Conventions for every call:
+ *   - Tensor arguments are DEVICE pointers (memory of the device the handle was
+ *     created on) unless the argument says "host".
+ *   - Floating-point tensors crossing the boundary are float32, row-major.
+ *     Weights are bfloat16 bit patterns (uint16_t), row-major [out, in].
+ *   - Work is enqueued on `stream` (0 = legacy default stream); calls return
+ *     without synchronising unless stated. The caller owns every buffer it
+ *     passes; the library never keeps a caller pointer after a call returns.
+ *   - Errors are returned, never thrown; qi_last_error() gives the calling
+ *     thread's last message. Device-side wait timeouts (which are bugs, not
+ *     expected events) are latched in a device error word and reported by
+ *     qi_dit_check() and by the next qi_dit_* call that synchronises.
+ *   - Calls on one qi_dit handle must not overlap across streams or threads.
+ */
+#ifndef QIDIT_H
+#define QIDIT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* qi_stream_t; /* same handle as cudaStream_t */
+
+typedef enum qi_status {
+  QI_OK = 0,
+  QI_ERR_INVALID_ARG = 1,     /* NULL pointer, bad enum, bad block index        */
+  QI_ERR_SHAPE = 2,           /* L, N, h, w out of range or over the handle's max */
+  QI_ERR_STATE = 3,           /* e.g. USE_CACHE with no valid capture for this L */
+  QI_ERR_OOM = 4,             /* device allocation failed                       */
+  QI_ERR_CUDA = 5,            /* a CUDA runtime/driver call failed              */
+  QI_ERR_DEVICE_TIMEOUT = 6,  /* a kernel's bounded wait expired (device word)  */
+  QI_ERR_NOT_IMPLEMENTED = 7
+} qi_status;
+
+/* Model widths [ARCH]. head_dim 128 follows from the 64 RoPE columns per token
+ * (one column per rotated pair); SwiGLU width 12288 = 3 x 4096. */
+#define QI_HIDDEN 4096
+#define QI_HEADS 32
+#define QI_HEAD_DIM 128
+#define QI_FFN 12288
+#define QI_MOD (4 * QI_HIDDEN) /* (s1, g1, s2, g2) */
+#define QI_PATCH 64            /* latent channels per image token */
+#define QI_TDIM 256            /* sinusoidal timestep width       */
+#define QI_BLOCKS 32
+#define QI_ROPE_COLS 64        /* 8 + 28 + 28 pairs per token     */
+#define QI_ROPE_POS_LO (-1024)
+#define QI_ROPE_NPOS 9216      /* positions -1024..8191           */
+
+/* Accepted sizes. L is the prompt length after the template prefix is dropped
+ * [HOST s2]; N = h*w image tokens. The pages' N axis stops at 4096 but their
+ * 2048^2 default is 16384 tokens, so N goes to 16384 here. */
+#define QI_L_MIN 1
+#define QI_L_MAX 512
+#define QI_N_MIN 1
+#define QI_N_MAX 16384
+
+/* qi_dit_step flags */
+#define QI_STEP_JOINT 0u      /* text + image rows; (re)captures the text K/V       */
+#define QI_STEP_USE_CACHE 1u  /* image rows only; text K/V come from the capture    */
+#define QI_STEP_HOST_IO 2u    /* img_tokens, txt_feats, cos/sin, vel are HOST ptrs  */
+
+typedef struct qi_dit qi_dit;
+
+typedef struct qi_dit_config {
+  int blocks; /* 1..32 (32 for the real model; fewer for tests)                 */
+  int L_max;  /* largest prompt length this handle serves (1..512)              */
+  int N_max;  /* largest image token count this handle serves (1..16384)        */
+} qi_dit_config;
+
+/* Global (non-block) tensors, bf16 bits, [out, in] row-major. */
+typedef struct qi_global_weights {
+  const uint16_t* t_w1;       /* [4096, 256]  timestep MLP, first Linear        */
+  const uint16_t* t_b1;       /* [4096]                                        */
+  const uint16_t* t_w2;       /* [4096, 4096] timestep MLP, second Linear       */
+  const uint16_t* t_b2;       /* [4096]                                        */
+  const uint16_t* mod_w;      /* [16384, 4096] the one shared modulation Linear */
+  const uint16_t* mod_b;      /* [16384]                                       */
+  const uint16_t* txt_norm_w; /* [4096] ZeroCenterRMSNorm gain w (scale 1 + w)  */
+  const uint16_t* txt_w;      /* [4096, 4096] text projection                   */
+  const uint16_t* txt_b;      /* [4096]                                        */
+  const uint16_t* img_w;      /* [4096, 64] image-token projection              */
+  const uint16_t* img_b;      /* [4096]                                        */
+  const uint16_t* out_w;      /* [64, 4096] proj_out                            */
+  const uint16_t* out_b;      /* [64]                                          */
+} qi_global_weights;
+
+/* One block's matrices, bf16 bits, [out, in] row-major. No biases. */
+typedef struct qi_block_weights {
+  const uint16_t* wq; /* [4096, 4096]  */
+  const uint16_t* wk; /* [4096, 4096]  */
+  const uint16_t* wv; /* [4096, 4096]  */
+  const uint16_t* wo; /* [4096, 4096]  */
+  const uint16_t* wg; /* [12288, 4096] SwiGLU gate */
+  const uint16_t* wu; /* [12288, 4096] SwiGLU up   */
+  const uint16_t* wd; /* [4096, 12288] SwiGLU down */
+} qi_block_weights;
+
+/* Sampler constants [HOST s6, scheduler.json]. */
+typedef struct qi_sched_params {
+  double base_shift;     /* 0.5  */
+  double max_shift;      /* 0.9  */
+  int base_seq;          /* 256  */
+  int max_seq;           /* 8192 */
+  double shift_terminal; /* 0.02 */
+  int train_steps;       /* 1000 */
+} qi_sched_params;
+
+/* ------------------------------------------------------------------ lifetime */
+
+/* Create a handle on CUDA device `device`: allocates the bf16 weight store
+ * (~14.2 GB at 32 blocks), activations for L_max + N_max rows and the per-block
+ * text K/V store. Weights start undefined: load them with qi_dit_load_*.
+ * Errors: INVALID_ARG (NULL), SHAPE (config out of range), OOM, CUDA. */
+qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out);
+
+/* Free everything the handle owns. Synchronises the device. NULL is a no-op. */
+qi_status qi_dit_destroy(qi_dit* dit);
+
+/* Copy the global tensors into the handle. `src_on_device` = 1 when the
+ * pointers are device memory, 0 when host memory. Returns after the copies
+ * completed, so the caller may free its copy. */
+qi_status qi_dit_load_global(qi_dit* dit, const qi_global_weights* w, int src_on_device,
+                             qi_stream_t stream);
+
+/* Copy block `block`'s matrices into the handle (repacked internally: Q|K|V
+ * stacked, gate/up interleaved by 128-row groups). Returns after completion. */
+qi_status qi_dit_load_block(qi_dit* dit, int block, const qi_block_weights* w,
+                            int src_on_device, qi_stream_t stream);
+
+/* ------------------------------------------------------------------ host contract */
+
+/* The three RoPE axis tables [HOST s4]: for axis widths d = 16, 56, 56 and
+ * positions p = -1024..8191 (row p + 1024), column k < d/2 holds
+ * cos/sin(fl32(fl32(p) * omega_k)), omega_k = fl32(theta^(-2k/d)); each value
+ * is the float32 rounding of the float64 cos/sin. Outputs (device, float32):
+ * cos0/sin0 [9216, 8], cos1/sin1 [9216, 28], cos2/sin2 [9216, 28]. */
+qi_status qi_rope_axis_tables(float theta, float* cos0, float* sin0, float* cos1, float* sin1,
+                              float* cos2, float* sin2, qi_stream_t stream);
+
+/* Per-token RoPE rows [HOST s4]: text token i has position (i, i, i); image
+ * token y*w + x has (L, y - (h - h/2), x - (w - w/2)); a token's 64 columns are
+ * the axis-0, axis-1, axis-2 rows concatenated (8 + 28 + 28), same values as
+ * qi_rope_axis_tables. Outputs (device, float32): txt_cos/txt_sin [L, 64],
+ * img_cos/img_sin [h*w, 64]. Any of the four may be NULL (skipped).
+ * Errors: SHAPE if L or h*w is out of range. */
+qi_status qi_rope_tables(int L, int h, int w, float theta, float* txt_cos, float* txt_sin,
+                         float* img_cos, float* img_sin, qi_stream_t stream);
+
+/* FlowMatch Euler schedule [HOST s6], computed on the host:
+ * s = linspace(1, 1/steps, steps); mu = N*m + b (m, b from the constants);
+ * s = e^mu / (e^mu + 1/s - 1); s = 1 - (1 - s) / ((1 - s_last) / (1 - shift_terminal));
+ * evaluated in float64, then timesteps[i] = fl32(s_i * train_steps) and
+ * sigmas = fl32(s) ++ [0]. `p` may be NULL (the constants above).
+ * Outputs (HOST): sigmas [steps + 1], timesteps [steps]. The DiT's timestep input
+ * for step i is fl32(timesteps[i] / 1000). Errors: INVALID_ARG, SHAPE (steps < 2: with a
+ * single step its only sigma is 1 and the terminal stretch divides 0 by 0). */
+qi_status qi_flow_sigmas(int steps, int N, const qi_sched_params* p, float* sigmas,
+                         float* timesteps);
+
+/* Noise packing [HOST s5]: x[y*w + x, c] = z[c, y, x] for a channel-major
+ * latent z [64, h, w] (device) into tokens x [h*w, 64] (device). */
+qi_status qi_pack_noise(const float* z, int h, int w, float* x, qi_stream_t stream);
+
+/* Euler update [HOST s6]: x <- x + (sigma_next - sigma_i) * vel, float32, the
+ * difference, the product and the sum each rounded on its own (no FMA).
+ * x, vel: device [N, 64]. */
+qi_status qi_euler_update(float* x, const float* vel, int N, float sigma_i, float sigma_next,
+                          qi_stream_t stream);
+
+/* ------------------------------------------------------------------ DiT */
+
+/* One DiT forward pass [ARCH; HOST s1]: vel [N, 64] from img_tokens [N, 64],
+ * txt_feats [L, 4096], the scalar timestep (t = timesteps[i] / 1000) and the
+ * per-token RoPE rows txt_cos/txt_sin [L, 64], img_cos/img_sin [N, 64].
+ *
+ * flags = QI_STEP_JOINT: all L + N rows run through every block; the text K/V
+ *   of every block are stored in the handle (the capture), valid for this L.
+ * flags = QI_STEP_USE_CACHE [REUSE]: only the N image rows run; attention reads
+ *   the stored text K/V. txt_feats and txt_cos/txt_sin may be NULL. The result
+ *   equals the joint pass's image rows bit for bit (every GEMM computes a row
+ *   independently of the others, and attention walks keys in the same order).
+ *   Errors: STATE if no capture is valid for this L.
+ * | QI_STEP_HOST_IO: the tensor pointers are host memory; the library copies
+ *   them in and vel out on `stream`, and synchronises it before returning.
+ * Errors: INVALID_ARG, SHAPE (L > L_max, N > N_max, ...), STATE, CUDA. */
+qi_status qi_dit_step(qi_dit* dit, const float* img_tokens, int N, const float* txt_feats, int L,
+                      float timestep, const float* txt_cos, const float* txt_sin,
+                      const float* img_cos, const float* img_sin, float* vel, unsigned flags,
+                      qi_stream_t stream);
+
+/* Text-only pass [REUSE]: run the L text rows (t = 0 modulation, causal over
+ * text) through every block and store their K/V, the same values a joint pass
+ * stores. No velocity. Marks the capture valid for this L. */
+qi_status qi_text_kv_capture(qi_dit* dit, const float* txt_feats, int L, const float* txt_cos,
+                             const float* txt_sin, qi_stream_t stream);
+
+/* Bytes of text K/V storage for `blocks` blocks and L tokens [REUSE]:
+ * 2 x blocks x L x 4096 x 2. */
+size_t qi_kv_cache_bytes(int blocks, int L);
+
+/* Device error word: synchronises `stream`, returns DEVICE_TIMEOUT (and clears
+ * the word) if a kernel's bounded wait expired since the last check. */
+qi_status qi_dit_check(qi_dit* dit, qi_stream_t stream);
+
+/* ------------------------------------------------------------------ test hooks */
+
+/* One block in the joint layout: hidden [L + N, 4096] float32 in/out (text rows
+ * first), modulation rows for t_img (image rows) and 0 (text rows), per-row
+ * RoPE cos/sin [L + N, 64]. Stores the block's K/V like a joint step. */
+qi_status qi_dit_block_forward(qi_dit* dit, int block, float* hidden, int L, int N, float t_img,
+                               const float* cos, const float* sin, qi_stream_t stream);
+
+/* Copy rows [row0, row0 + rows) of block `block`'s stored K and V (bf16 bits,
+ * [rows, 4096] each, device) into k_out / v_out. After a pass, rows [0, L) are
+ * the text K/V (post-RoPE K) and rows [L, L + N) the image K/V of that pass.
+ * Errors: INVALID_ARG (block, NULL), SHAPE (rows past L_max + N_max). */
+qi_status qi_dit_read_kv(qi_dit* dit, int block, int row0, int rows, uint16_t* k_out, uint16_t* v_out,
+                         qi_stream_t stream);
+
+/* The block's tensor-core GEMM on its own, plain fp32 output (test hook):
+ * D[M, N] = A[M, K] * B[N, K]^T with A, B bf16 bits row-major (device).
+ * Requires N % 256 == 0, K % 64 == 0, 16-byte aligned A and B; M >= 1 any.
+ * Uses the handle's device error word. Errors: SHAPE, INVALID_ARG, CUDA. */
+qi_status qi_gemm_bf16(qi_dit* dit, const uint16_t* A, const uint16_t* B, float* D, int M, int N, int K,
+                       qi_stream_t stream);
+
+/* The block-causal attention kernel on its own (test hook). q [Rq, 4096],
+ * k/v [Lk, 4096], o [Rq, 4096], bf16 bits, 32 heads x 128 (device). Query row
+ * r has global index r + q_off: if that is < L it sees keys 0..index (text,
+ * causal), otherwise keys 0..Lk-1. Scale 1/sqrt(128). */
+qi_status qi_attention_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, int Rq,
+                            int q_off, int L, int Lk, qi_stream_t stream);
+
+/* During later qi_dit_step calls, copy the float32 residual stream entering
+ * block `block` ([R, 4096], R = rows of that pass; `block` = blocks means the
+ * stream after the last block) into `dst` (device). slot 0 or 1; dst NULL clears. */
+qi_status qi_dit_set_trace(qi_dit* dit, int slot, int block, float* dst);
+
+/* Per-kernel-class device time, measured with CUDA events on the launching
+ * stream while enabled. Classes: 0 QKV GEMM, 1 attention, 2 out-proj GEMM,
+ * 3 gate/up GEMM, 4 down GEMM, 5 other. */
+#define QI_PROF_CLASSES 6
+qi_status qi_dit_profile(qi_dit* dit, int enable);
+/* Synchronises; writes total milliseconds and launch counts per class since
+ * the last reset, then resets. ms/launches: host arrays [QI_PROF_CLASSES]. */
+qi_status qi_dit_profile_read(qi_dit* dit, double* ms, long long* launches);
+
+/* Message for the calling thread's last failed call ("" if none). */
+const char* qi_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QIDIT_H */

@@ -1,0 +1,47 @@
+"""Helpers shared by the GPU tests: metrics, the tolerance, weight upload."""
+import numpy as np
+
+import synth
+
+# Floating-point bar for bf16-GEMM / fp32-accumulate compute against the fp32
+# oracle: per-row cosine >= 0.999 and max|diff| / max|ref| <= 2e-2.
+COS_MIN = 0.999
+REL_MAX = 2e-2
+
+
+def row_cos(a, b):
+    a = np.asarray(a, np.float64).reshape(a.shape[0], -1)
+    b = np.asarray(b, np.float64).reshape(b.shape[0], -1)
+    num = (a * b).sum(1)
+    den = np.sqrt((a * a).sum(1) * (b * b).sum(1)) + 1e-300
+    return num / den
+
+
+def rel_max(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return float(np.abs(got - ref).max() / np.abs(ref).max())
+
+
+def assert_close(got, ref, what, cos_min=COS_MIN, rel=REL_MAX):
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    c = row_cos(got, ref)
+    r = rel_max(got, ref)
+    assert c.min() >= cos_min and r <= rel, f"{what}: min row cos {c.min():.6f}, max rel {r:.3e}"
+    return c.min(), r
+
+
+def load_weights(dit, W: "synth.Weights"):
+    dit.load_global(W.glob)
+    for b in range(dit.blocks):
+        dit.load_block(b, W.block(b))
+
+
+def bf16_tensor(bits, device="cuda"):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device)
+
+
+def f32_tensor(a, device="cuda"):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)

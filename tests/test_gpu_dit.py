@@ -1,0 +1,128 @@
+"""GPU parity of the DiT block and the full step against the oracle (C ABI)."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import dit as odit
+from oracle import rope as orope
+
+from gpu_util import assert_close, f32_tensor, load_weights
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qi():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import diffusion_transformer_text_gb300 as q
+    q.build()
+    q.lib()
+    return q
+
+
+def _tables(L, h, w):
+    tc, ts, ic, is_ = orope.token_tables(L, h, w)
+    return tc, ts, ic, is_
+
+
+# ---------------------------------------------------------------- one block
+
+def test_one_block(qi):
+    """One block at full width: hidden [72, 4096], L = 8 text rows then an 8x8 grid."""
+    case = synth.BLOCK_CASE
+    W = synth.Weights(seed=case.seed, nblocks=1)
+    d = qi.DiT(blocks=1, L_max=case.L, N_max=case.N)
+    try:
+        load_weights(d, W)
+        x = synth.block_hidden(case)
+        tc, ts, ic, is_ = _tables(case.L, case.h, case.w)
+        cos, sin = np.concatenate([tc, ic]), np.concatenate([ts, is_])
+        mods = odit.row_mods(odit.modulation(W.glob, case.timestep), odit.modulation(W.glob, 0.0), case.L,
+                             case.L + case.N)
+        ref, rk, rv = odit.block_forward(W.block(0), x, mods, case.L, cos, sin, 32, return_kv=True)
+        got = d.block_forward(0, f32_tensor(x), case.L, case.timestep, f32_tensor(cos), f32_tensor(sin))
+        d.check()
+        got = got.cpu().numpy()
+        # the residual carries the input through; judge the block's update
+        assert_close(got - x, ref - x, "block update")
+        k, v = d.read_kv(0, 0, case.L + case.N)
+        k = synth.bf16_bits_to_f32(k.cpu().numpy().view(np.uint16))
+        v = synth.bf16_bits_to_f32(v.cpu().numpy().view(np.uint16))
+        assert_close(k, rk.reshape(case.L + case.N, -1), "stored K (post-RoPE)")
+        assert_close(v, rv.reshape(case.L + case.N, -1), "stored V")
+    finally:
+        d.close()
+
+
+# ---------------------------------------------------------------- full step, 256^2
+
+@pytest.fixture(scope="module")
+def dit256(qi):
+    case = synth.STEP_256
+    W = synth.Weights(seed=case.seed)
+    d = qi.DiT(blocks=32, L_max=case.L, N_max=case.N)
+    load_weights(d, W)
+    yield case, W, d
+    d.close()
+
+
+def test_step_256(qi, dit256):
+    case, W, d = dit256
+    img = synth.img_tokens(case)
+    txt = synth.txt_feats(case)
+    tc, ts, ic, is_ = _tables(case.L, case.h, case.w)
+    vel = d.step(f32_tensor(img), f32_tensor(txt), case.timestep, f32_tensor(tc), f32_tensor(ts), f32_tensor(ic),
+                 f32_tensor(is_))
+    d.check()
+    ref = odit.dit_forward(W, img, txt, np.float32(case.timestep), tc, ts, ic, is_)
+    assert_close(vel.cpu().numpy(), ref, "vel 256^2")
+
+
+def test_reuse_equals_joint_bit_exact(qi, dit256):
+    """Image-only steps over the captured text K/V reproduce the joint pass exactly."""
+    case, W, d = dit256
+    img = f32_tensor(synth.img_tokens(case))
+    txt = f32_tensor(synth.txt_feats(case))
+    tc, ts, ic, is_ = [f32_tensor(a) for a in _tables(case.L, case.h, case.w)]
+    for t in (0.97, 0.41):
+        joint = d.step(img, txt, t, tc, ts, ic, is_).clone()
+        cached = d.step_cached(img, case.L, t, ic, is_)
+        d.check()
+        assert np.array_equal(joint.cpu().numpy(), cached.cpu().numpy())
+    # a different image at another t still matches its own joint pass
+    img2 = f32_tensor(synth.input_f32(case.seed, 77, (case.N, 64)))
+    c2 = d.step_cached(img2, case.L, 0.2, ic, is_).clone()
+    j2 = d.step(img2, txt, 0.2, tc, ts, ic, is_)
+    assert np.array_equal(c2.cpu().numpy(), j2.cpu().numpy())
+
+
+def test_text_only_capture_equals_joint(qi, dit256):
+    """A text-only pass stores the same text K/V as a joint pass, bit for bit."""
+    case, W, d = dit256
+    img = f32_tensor(synth.img_tokens(case))
+    txt = f32_tensor(synth.txt_feats(case))
+    tc, ts, ic, is_ = [f32_tensor(a) for a in _tables(case.L, case.h, case.w)]
+    d.step(img, txt, 0.97, tc, ts, ic, is_)
+    joint = [tuple(t.cpu().numpy() for t in d.read_kv(b, 0, case.L)) for b in (0, 13, 31)]
+    d.text_kv_capture(txt, tc, ts)
+    d.check()
+    for (jk, jv), b in zip(joint, (0, 13, 31)):
+        k, v = d.read_kv(b, 0, case.L)
+        assert np.array_equal(jk, k.cpu().numpy()) and np.array_equal(jv, v.cpu().numpy())
+
+
+def test_use_cache_requires_capture(qi):
+    d = qi.DiT(blocks=1, L_max=8, N_max=64)
+    try:
+        import torch
+        img = torch.zeros(64, 64, device="cuda")
+        cs = torch.zeros(64, 64, device="cuda")
+        W = synth.Weights(seed=0, nblocks=1)
+        load_weights(d, W)
+        with pytest.raises(qi.QiError) as e:
+            d.step_cached(img, 8, 0.5, cs, cs)
+        assert e.value.status == 3
+    finally:
+        d.close()

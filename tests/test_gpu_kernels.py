@@ -1,0 +1,138 @@
+"""GPU parity of the individual kernels against the oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import attention as oatt
+from oracle import rope as orope
+from oracle import sched as osched
+
+from gpu_util import assert_close, bf16_tensor, f32_tensor
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qi():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import diffusion_transformer_text_gb300 as q
+    q.build()
+    q.lib()
+    return q
+
+
+@pytest.fixture(scope="module")
+def small_dit(qi):
+    d = qi.DiT(blocks=1, L_max=16, N_max=64)
+    yield d
+    d.close()
+
+
+# ---------------------------------------------------------------- GEMM
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 64), (200, 512, 256), (300, 768, 4096), (129, 256, 12288)])
+def test_gemm_matches_matmul(qi, small_dit, M, N, K):
+    A = synth.weight_bf16(10, M, (M, K), std=1.0)
+    B = synth.weight_bf16(11, N, (N, K), std=1.0)
+    D = small_dit.gemm(bf16_tensor(A), bf16_tensor(B)).cpu().numpy()
+    small_dit.check()
+    a = synth.bf16_bits_to_f32(A).astype(np.float64)
+    b = synth.bf16_bits_to_f32(B).astype(np.float64)
+    ref = a @ b.T
+    # bf16 products are exact in fp32; only the fp32 accumulation rounds. Bound the
+    # error elementwise by a small multiple of sum_k |a_k b_k| (far below K * 2^-24).
+    bound = 1e-5 * (np.abs(a) @ np.abs(b).T) + 1e-6
+    assert (np.abs(D - ref) <= bound).all(), float((np.abs(D - ref) / bound).max())
+
+
+def test_gemm_rows_independent_of_m(qi, small_dit):
+    """A row's result does not depend on how many rows the pass has (exact)."""
+    K = 4096
+    A = synth.weight_bf16(12, 0, (300, K), std=1.0)
+    B = synth.weight_bf16(13, 0, (512, K), std=1.0)
+    full = small_dit.gemm(bf16_tensor(A), bf16_tensor(B)).cpu().numpy()
+    part = small_dit.gemm(bf16_tensor(A[170:200]), bf16_tensor(B)).cpu().numpy()
+    assert np.array_equal(full[170:200], part)
+
+
+# ---------------------------------------------------------------- attention
+
+def _qkv(R, seed):
+    q = synth.weight_bf16(seed, 0, (R, 4096), std=1.3)
+    k = synth.weight_bf16(seed, 1, (R, 4096), std=1.3)
+    v = synth.weight_bf16(seed, 2, (R, 4096), std=1.0)
+    return q, k, v
+
+
+def _oracle_att(q, k, v, L):
+    R = q.shape[0]
+    f = lambda a: synth.bf16_bits_to_f32(a).reshape(R, 32, 128)
+    return oatt.attention_masked(f(q), f(k), f(v), L)
+
+
+@pytest.mark.parametrize("L,N", [(7, 150), (1, 64), (130, 70), (22, 256)])
+def test_attention_joint(qi, L, N):
+    q, k, v = _qkv(L + N, L + N)
+    o = qi.attention(bf16_tensor(q), bf16_tensor(k), bf16_tensor(v), L)
+    got = synth.bf16_bits_to_f32(o.cpu().numpy().view(np.uint16))
+    ref = _oracle_att(q, k, v, L)
+    assert_close(got.reshape(L + N, -1), ref, f"attention L={L} N={N}")
+
+
+def test_attention_image_only_equals_joint(qi):
+    """Image rows against stored text K/V give the joint pass's image rows bit for bit."""
+    L, N = 37, 200
+    q, k, v = _qkv(L + N, 5)
+    qt, kt, vt = bf16_tensor(q), bf16_tensor(k), bf16_tensor(v)
+    joint = qi.attention(qt, kt, vt, L).cpu().numpy()
+    img = qi.attention(qt[L:].contiguous(), kt, vt, L, q_off=L).cpu().numpy()
+    assert np.array_equal(joint[L:], img)
+    # and the text rows of a text-only pass equal the joint pass's text rows
+    txt = qi.attention(qt[:L].contiguous(), kt[:L].contiguous(), vt[:L].contiguous(), L).cpu().numpy()
+    assert np.array_equal(joint[:L], txt)
+
+
+def test_attention_long_keys(qi):
+    """Several query and key tiles with a ragged tail at a realistic head count."""
+    L, N = 407, 600
+    q, k, v = _qkv(L + N, 9)
+    o = qi.attention(bf16_tensor(q), bf16_tensor(k), bf16_tensor(v), L)
+    got = synth.bf16_bits_to_f32(o.cpu().numpy().view(np.uint16))
+    assert_close(got, _oracle_att(q, k, v, L), "attention 407+600")
+
+
+# ---------------------------------------------------------------- RoPE, Euler, packing
+
+def test_rope_axis_tables_bit_exact(qi):
+    got = qi.rope_axis_tables(10000.0)
+    ref = orope.axis_tables()
+    for (gc, gs), (rc, rs) in zip(got, ref):
+        assert np.array_equal(gc.cpu().numpy(), rc)
+        assert np.array_equal(gs.cpu().numpy(), rs)
+
+
+@pytest.mark.parametrize("L,h,w", [(8, 8, 8), (22, 16, 16), (407, 64, 64), (512, 128, 128), (3, 5, 7)])
+def test_rope_token_tables_bit_exact(qi, L, h, w):
+    got = [t.cpu().numpy() for t in qi.rope_tables(L, h, w)]
+    ref = orope.token_tables(L, h, w)
+    for g, r in zip(got, ref):
+        assert g.tobytes() == r.tobytes()
+
+
+@pytest.mark.parametrize("N", [1, 255, 4096])
+def test_euler_bit_exact(qi, N):
+    x = synth.input_f32(3, 50, (N, 64))
+    v = synth.input_f32(3, 51, (N, 64))
+    s, _ = osched.flow_sigmas(40, 4096)
+    xt = f32_tensor(x)
+    qi.euler_update(xt, f32_tensor(v), float(s[7]), float(s[8]))
+    assert xt.cpu().numpy().tobytes() == osched.euler_update(x, v, s[7], s[8]).tobytes()
+
+
+@pytest.mark.parametrize("h,w", [(8, 8), (64, 64), (5, 3)])
+def test_pack_noise_exact(qi, h, w):
+    z = synth.input_f32(4, 2, (64, h, w))
+    x = qi.pack_noise(f32_tensor(z)).cpu().numpy()
+    assert np.array_equal(x, orope.pack_noise(z))
