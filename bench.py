@@ -10,7 +10,7 @@ Euler update. K timed steps run images back to back from step 0.
 Prints one JSON line (rank 0). Under torchrun each rank runs an independent
 replica on its own GPU (the step has no exchange between images): weak scaling.
 The reference arm times the CPU oracle on this host's cores on a bounded sample
-(one block of the joint 1024^2 pass per bench step, scaled to 32 blocks).
+(per bench step, 512 image rows of one 1024^2 block; 256 such slices make a step).
 """
 from __future__ import annotations
 
@@ -121,8 +121,20 @@ class Clocks:
 # ----------------------------------------------------------------------------- oracle (CPU)
 
 
+SAMPLE_ROWS = 512
+SAMPLES_PER_STEP = (N // SAMPLE_ROWS) * BLOCKS  # oracle slices that make one image-only step
+
+
 def oracle_block_sample(samples: int, seed: int = CASE.seed):
-    """Time the oracle on `samples` joint-pass blocks at 1024^2; returns seconds per block."""
+    """Time the oracle on `samples` slices of an image-only 1024^2 block.
+
+    A slice is 512 image rows of one block: their QKV projection and RoPE,
+    attention over all L + N keys (image rows see every key, so the oracle's
+    plain SDPA applies) and the out-projection and SwiGLU MLP. The block's K/V
+    over all rows are computed once beforehand, as the sampler would hold them.
+    One image-only step is SAMPLES_PER_STEP such slices. Returns seconds per slice.
+    """
+    from oracle import attention as oatt
     from oracle import dit as odit
     from oracle import rope as orope
     Wt = synth.Weights(seed=seed, nblocks=1)
@@ -131,10 +143,16 @@ def oracle_block_sample(samples: int, seed: int = CASE.seed):
     tc, ts, ic, is_ = orope.token_tables(L, H, W_)
     cos, sin = np.concatenate([tc, ic]), np.concatenate([ts, is_])
     mods = odit.row_mods(odit.modulation(Wt.glob, 0.5), odit.modulation(Wt.glob, 0.0), L, L + N)
+    s1, g1, s2, g2 = odit.mod_chunks(mods)
+    _, k, v = odit.block_qkv(bw, x, s1, cos, sin, 32)
     times = []
-    for _ in range(samples):
+    for i in range(samples):
+        lo = L + (i * SAMPLE_ROWS) % N
+        rows = slice(lo, lo + SAMPLE_ROWS)
         t0 = time.perf_counter()
-        odit.block_forward(bw, x, mods, L, cos, sin, 32)
+        q, _, _ = odit.block_qkv(bw, x[rows], s1[rows], cos[rows], sin[rows], 32)
+        o = oatt.sdpa(q, k, v, causal=False).reshape(SAMPLE_ROWS, HIDDEN)
+        odit.block_after_attention(bw, x[rows], o, g1[rows], s2[rows], g2[rows])
         times.append(time.perf_counter() - t0)
     return times
 
@@ -156,18 +174,19 @@ def run_reference(args, rank, world):
     nsamp = args.warmup + args.steps
     times = oracle_block_sample(nsamp)
     timed = times[args.warmup:]
-    per_step = float(np.mean(timed)) * BLOCKS
+    per_step = float(np.mean(timed)) * SAMPLES_PER_STEP
     value = 1.0 / per_step
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "1024^2 sampler step, N=4096, L=407 (dense joint pass)", "global_batch": 1,
+        "config": {"workload": "1024^2 image-only sampler step, N=4096, L=407, 32 blocks", "global_batch": 1,
                    "seq_len": L + N, "parallelism": "none"},
         "impl": "reference",
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores_used(), "kind": "oracle",
-                         "sample": f"one oracle block (numpy fp32) of the joint 1024^2 pass per bench step, "
-                                   f"x32 blocks; {len(timed)} timed samples"},
+                         "sample": f"per bench step one oracle slice (numpy fp32): 512 image rows of one "
+                                   f"block with precomputed K/V; a step is {SAMPLES_PER_STEP} slices; "
+                                   f"{len(timed)} timed slices"},
         "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -237,7 +256,12 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     dit.check()
 
-    clocks = Clocks(local_rank)
+    try:  # nvidia-smi ignores CUDA_VISIBLE_DEVICES: address the GPU by UUID
+        uuid = str(torch.cuda.get_device_properties(local_rank).uuid)
+        gpu_id = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+    except Exception:
+        gpu_id = str(local_rank)
+    clocks = Clocks(gpu_id)
     dit.profile(True)
     barrier()
     torch.cuda.synchronize()
@@ -338,11 +362,12 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        times = oracle_block_sample(3)
-        per_step = float(np.mean(times[1:])) * BLOCKS
+        times = oracle_block_sample(9)
+        per_step = float(np.mean(times[1:])) * SAMPLES_PER_STEP
         line["cpu_baseline"] = {"value": 1.0 / per_step, "unit": "steps/s", "cores": cores_used(),
                                 "kind": "oracle",
-                                "sample": "2 timed oracle blocks (numpy fp32, dense joint 1024^2 pass), x32 blocks"}
+                                "sample": f"8 timed oracle slices (numpy fp32, 512 image rows of one 1024^2 block "
+                                          f"each, K/V precomputed), scaled by {SAMPLES_PER_STEP} slices per step"}
     dit.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
