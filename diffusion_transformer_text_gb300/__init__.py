@@ -38,7 +38,7 @@ SYMBOLS = (
     "qi_rope_axis_tables", "qi_rope_tables", "qi_flow_sigmas", "qi_pack_noise", "qi_euler_update",
     "qi_dit_step", "qi_text_kv_capture", "qi_kv_cache_bytes", "qi_dit_check",
     "qi_dit_block_forward", "qi_dit_read_kv", "qi_dit_set_trace", "qi_dit_profile",
-    "qi_dit_profile_read", "qi_last_error", "qi_gemm_bf16", "qi_attention_bf16",
+    "qi_dit_profile_read", "qi_last_error", "qi_gemm_bf16", "qi_attention_bf16", "qi_gemm_bf16_noalloc",
 )
 
 
@@ -103,6 +103,7 @@ def lib() -> ctypes.CDLL:
         "qi_dit_profile_read": [P, P, P],
         "qi_gemm_bf16": [P, P, P, P, I, I, I, P],
         "qi_attention_bf16": [P, P, P, P, I, I, I, I, P],
+        "qi_gemm_bf16_noalloc": [P, P, P, I, I, I, I, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)

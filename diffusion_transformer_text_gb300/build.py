@@ -19,7 +19,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libqidit.so")
-SOURCES = ["qidit.cu", "gemm.cu", "attention.cu", "kernels_small.cu"]
+SOURCES = ["qidit.cu", "gemm.cu", "attention.cu", "kernels_small.cu", "gemm_noalloc.cu"]
 HEADERS = ["ptx.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

@@ -95,4 +95,7 @@ cudaError_t launch_rope_tokens(int L, int h, int w, float theta, float* tc, floa
                                cudaStream_t s);
 cudaError_t launch_pack_noise(const float* z, int h, int w, float* x, cudaStream_t s);
 
+// Sets the calling thread's message returned by qi_last_error() (qidit.cu).
+void set_last_error(const char* msg);
+
 }  // namespace qi

@@ -361,6 +361,8 @@ bool all_loaded(const qi_dit* d) {
 
 }  // namespace
 
+void qi::set_last_error(const char* msg) { g_last_error = msg; }
+
 // ================================================================ C ABI
 
 extern "C" {

@@ -247,6 +247,26 @@ qi_status qi_dit_read_kv(qi_dit* dit, int block, int row0, int rows, uint16_t* k
 qi_status qi_gemm_bf16(qi_dit* dit, const uint16_t* A, const uint16_t* B, float* D, int M, int N, int K,
                        qi_stream_t stream);
 
+/* qi_gemm_bf16 without a handle and without allocating. The pages have no
+ * counterpart: this exists for callers that may not call the CUDA allocator,
+ * such as code inside a host that owns all device memory (an inference server
+ * with a fixed arena, a plugin barred from cudaMalloc); they cannot create a
+ * qi_dit handle, whose creation allocates the weight store and work buffers.
+ * Same kernel, same result as qi_gemm_bf16: D[M, N] = A[M, K] * B[N, K]^T,
+ * bf16 bits in, fp32 out, all device pointers owned by the caller.
+ * Scratch: the kernel's status word sits in a 256-byte static device array
+ * that the library holds on every device that loads it, until exit. The first
+ * call on a device (the device current at the call) looks the array up with
+ * cudaGetSymbolAddress; make that first call before any stream capture. Every
+ * call clears the status word, then the kernel reports into it, so calls that
+ * overlap on the GPU (other streams, other threads) race on it; serialise them.
+ * Limits: N % 256 == 0, K % 64 == 0, M <= 16896, N <= 24576, K <= 12288 (the
+ * DiT's own GEMM shapes); larger sizes return QI_ERR_SHAPE with a message in
+ * qi_last_error(). sync_check != 0 synchronises `stream` and returns
+ * QI_ERR_DEVICE_TIMEOUT if a bounded wait in the kernel expired. */
+qi_status qi_gemm_bf16_noalloc(const uint16_t* A, const uint16_t* B, float* D, int M, int N, int K,
+                               int sync_check, qi_stream_t stream);
+
 /* The block-causal attention kernel on its own (test hook). q [Rq, 4096],
  * k/v [Lk, 4096], o [Rq, 4096], bf16 bits, 32 heads x 128 (device). Query row
  * r has global index r + q_off: if that is < L it sees keys 0..index (text,
