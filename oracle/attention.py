@@ -75,6 +75,26 @@ def attention_two_segment(q, k, v, L: int) -> np.ndarray:
     return np.concatenate([txt, img], axis=0).reshape(R, H * D)
 
 
+def attention_rows(q_rows, rows, k, v, L: int) -> np.ndarray:
+    """The masked softmax for selected query rows only.
+
+    q_rows [n, H, D] are the queries of global rows `rows`; k, v [R, H, D] hold
+    every key row. Row i sees keys 0..i if i < L, else all R keys. Returns [n, H*D].
+    """
+    n, H, D = q_rows.shape
+    R = k.shape[0]
+    scale = np.float32(1.0 / math.sqrt(D))
+    out = np.empty((n, H, D), np.float32)
+    j = np.arange(R)
+    for h in range(H):
+        s = (q_rows[:, h, :] @ k[:, h, :].T) * scale
+        i = np.asarray(rows)[:, None]
+        allowed = ((i < L) & (j[None, :] <= i)) | (i >= L)
+        s = np.where(allowed, s, -np.inf).astype(np.float32)
+        out[:, h, :] = _softmax_rows(s) @ v[:, h, :]
+    return out.reshape(n, H * D)
+
+
 def attention_bruteforce(q, k, v, L: int):
     """Triple loop in Python floats (float64); for tiny shapes only."""
     R, H, D = q.shape

@@ -36,7 +36,7 @@ import numpy as np
 
 from synth import bf16_bits_to_f32
 
-from .attention import attention_masked
+from .attention import attention_masked, attention_rows
 
 EPS = 1e-6
 
@@ -142,6 +142,25 @@ def block_forward(bw: dict, x: np.ndarray, mods: np.ndarray, L: int, cos, sin, h
     if return_kv:
         return y, k, v
     return y
+
+
+def block_forward_rows(bw: dict, x: np.ndarray, mods: np.ndarray, L: int, cos, sin, heads: int, rows,
+                       kv=None):
+    """The block's output for selected global rows only.
+
+    Every row's K and V are still needed (x, mods, cos, sin cover all R rows);
+    pass `kv` = (k, v) [R, heads, D] to reuse them. Returns (out [n, H], (k, v)).
+    """
+    rows = np.asarray(rows)
+    s1, g1, s2, g2 = mod_chunks(mods)
+    if kv is None:
+        _, k, v = block_qkv(bw, x, s1, cos, sin, heads)
+    else:
+        k, v = kv
+    q, _, _ = block_qkv(bw, x[rows], s1[rows], cos[rows], sin[rows], heads)
+    o = attention_rows(q, rows, k, v, L)
+    out = block_after_attention(bw, x[rows], o, g1[rows], s2[rows], g2[rows])
+    return out, (k, v)
 
 
 def embed(g: dict, img_tokens, txt_feats):

@@ -57,6 +57,15 @@ def test_text_rows_ignore_image_rows():
     assert not np.array_equal(a[L:], b[L:])
 
 
+def test_selected_rows_equal_dense():
+    L, N, H, D = 6, 30, 2, 8
+    q, k, v = _qkv(L + N, H, D, seed=7)
+    dense = att.attention_masked(q, k, v, L)
+    rows = np.array([0, 3, 5, 6, 17, 35])
+    got = att.attention_rows(q[rows], rows, k, v, L)
+    assert np.abs(got - dense[rows]).max() <= 1e-6 * np.abs(dense).max()
+
+
 def test_first_text_row_copies_its_value():
     """Text row 0 sees only key 0, so its output is v[0] exactly."""
     L, N, H, D = 4, 5, 2, 8

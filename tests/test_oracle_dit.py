@@ -117,6 +117,21 @@ def test_block_matches_rowloop():
     assert np.abs(got - ref).max() <= 2e-5 * np.abs(ref - x).max()
 
 
+def test_block_rows_equal_dense_block():
+    """The selected-rows block (used for full-size sampled checks) equals the dense block."""
+    W = synth.Weights(seed=6, dims=TINY)
+    L, h, w = 4, 3, 3
+    R = L + h * w
+    tc, ts, ic, is_ = _tables(L, h, w, TINY)
+    cos, sin = np.concatenate([tc, ic]), np.concatenate([ts, is_])
+    mods = dit.row_mods(dit.modulation(W.glob, 0.7), dit.modulation(W.glob, 0.0), L, R)
+    x = synth.input_f32(6, 0, (R, TINY.hidden))
+    dense = dit.block_forward(W.block(0), x, mods, L, cos, sin, TINY.heads)
+    rows = [0, 2, 4, 9, 12]
+    got, _ = dit.block_forward_rows(W.block(0), x, mods, L, cos, sin, TINY.heads, rows)
+    assert np.abs(got - dense[rows]).max() <= 1e-6 * np.abs(dense).max()
+
+
 def test_dit_matches_loops():
     """Embedding, two blocks and the head, against loop forms (tiny width)."""
     W = synth.Weights(seed=7, dims=TINY)
