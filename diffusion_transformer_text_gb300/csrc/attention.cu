@@ -1,249 +1,292 @@
-// Block-causal flash attention for the single-stream DiT (first version,
-// warp-level mma.sync m16n8k16 bf16 with fp32 accumulation).
+// Block-causal flash attention on the 5th-generation tensor cores (tcgen05).
 //
 // Mask (no mask tensor): query row with global index i attends to key j iff
 //   (i < L and j <= i)  -- text rows are causal over text only
 //   (i >= L and j < Lk) -- image rows see every text and image key.
 // This is the port's "two SDPA calls" decomposition (text->text causal,
-// image->all) done in one pass. Keys are visited in 64-row tiles from key 0 in
+// image->all) done in one pass. Keys are visited in 128-row tiles from key 0 in
 // the same order whatever the query tile holds, so an image row's result is the
 // same in a joint pass and in an image-only pass over the stored text K/V.
 //
-// CTA: 128 query rows x one head (8 warps x 16 rows), K/V tiles of 64 keys
-// double-buffered in shared memory with cp.async, online softmax in base 2.
+// CTA = 128 query rows of one head; two CTAs share an SM (256 TMEM columns and
+// ~98 KB of shared memory each), so one CTA's softmax overlaps the other's MMAs.
+// Roles (192 threads):
+//   warp 0     TMA producer: Q once, then K and V tiles (128 keys x 128 dims)
+//   warp 1     TMEM owner and MMA issuer: S = Q K^T (M128 N128, both K-major),
+//              then O += P V with P read from TMEM and V MN-major in shared memory
+//   warps 2-5  softmax: thread = query row (TMEM lane). Reads its S row, keeps a
+//              running max (O is rescaled only when the max grows by more than
+//              2^8, the row sum uses the same max, so the result is unchanged),
+//              writes P as bf16 over the S columns, and at the end scales O by
+//              1 / rowsum and stores it.
+// Every mbarrier wait is bounded; on expiry the error word is set and the CTA
+// drains its copies and MMAs before releasing TMEM.
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace qi {
 namespace {
 
-constexpr int kBQ = 128;
-constexpr int kBKV = 64;
-constexpr int kD = kHeadDim;  // 128
-constexpr int kThreads = 256;
-constexpr int kTileQBytes = kBQ * kD * 2;    // 32 KB
-constexpr int kTileKVBytes = kBKV * kD * 2;  // 16 KB
-constexpr int kSmem = kTileQBytes + 4 * kTileKVBytes;
+constexpr int kBQ = 128;                       // query rows per CTA
+constexpr int kBKV = 128;                      // keys per tile
+constexpr int kHalfBytes = 128 * 64 * 2;       // one 128-row x 64-column swizzled box: 16 KB
+constexpr int kTileBytes = 2 * kHalfBytes;     // 128 rows x 128 dims: 32 KB
+constexpr int kSmem = 3 * kTileBytes + 1024 + 256;
+constexpr uint32_t kTmemCols = 256;            // S/P: columns [0,128), O: [128,256)
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128);
+constexpr uint32_t kIdescPV = idesc_bf16_f32_bmn(128, 128);
+constexpr float kRescaleLog2 = 8.0f;           // rescale O only when the max grows by > 2^8
 
-// byte offset of element (row, col) in a [rows][128] bf16 tile whose 16-byte
-// chunks are XOR-swizzled by (row & 7): conflict-free ldmatrix on 8 rows.
-__device__ __forceinline__ uint32_t swz(int row, int col) {
-  const int chunk = (col >> 3) ^ (row & 7);
-  return static_cast<uint32_t>(row * (kD * 2) + chunk * 16 + (col & 7) * 2);
-}
+__global__ void __launch_bounds__(192, 2)
+    attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+            const __grid_constant__ CUtensorMap tmV, const AttnParams p, float scale_log2) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + kTileBytes;
+  uint8_t* sV = smem + 2 * kTileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 3 * kTileBytes);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = bars + 2;
+  uint64_t* v_full = bars + 3;
+  uint64_t* v_empty = bars + 4;
+  uint64_t* s_full = bars + 5;
+  uint64_t* p_full = bars + 6;
+  uint64_t* o_done = bars + 7;
+  uint64_t* drain = bars + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
-  const int n = pred ? 16 : 0;  // n = 0 zero-fills the 16 bytes
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Load a [rows][128] bf16 tile (row stride kHidden elements) into swizzled smem.
-template <int ROWS>
-__device__ __forceinline__ void load_tile(uint32_t sbase, const __nv_bfloat16* g, int row0, int nrows, int col0) {
-  constexpr int kChunks = ROWS * (kD / 8);
-#pragma unroll
-  for (int i = 0; i < kChunks / kThreads; ++i) {
-    const int c = threadIdx.x + i * kThreads;
-    const int r = c >> 4;
-    const int ch = c & 15;
-    const bool ok = (row0 + r) < nrows;
-    const __nv_bfloat16* src = g + (ok ? static_cast<size_t>(row0 + r) * kHidden + col0 + ch * 8 : 0);
-    cp_async16(sbase + swz(r, ch * 8), src, ok);
-  }
-}
-
-__global__ void __launch_bounds__(kThreads, 1) attn_fwd(const AttnParams p, float scale_log2) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const uint32_t sQ = smem_u32(smem);
-  const uint32_t sK = sQ + kTileQBytes;                 // 2 buffers
-  const uint32_t sV = sK + 2 * kTileKVBytes;            // 2 buffers
-
-  const int head = blockIdx.y;
-  const int r0 = blockIdx.x * kBQ;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int g = lane >> 2;
-  const int t4 = lane & 3;
-  const int col0 = head * kD;
+  const int head = blockIdx.y;
+  const int r0 = blockIdx.x * kBQ;
+  const int col0 = head * kHeadDim;
 
-  // keys this CTA must visit
+  // keys this CTA visits: image rows need all Lk keys; a CTA of text rows only
+  // needs keys up to its last row.
   const int last_q = p.q_off + min(r0 + kBQ, p.Rq) - 1;
   const int kend = last_q >= p.L ? p.Lk : min(p.Lk, last_q + 1);
   const int ntiles = (kend + kBKV - 1) / kBKV;
 
-  load_tile<kBQ>(sQ, p.q, r0, p.Rq, col0);
-  load_tile<kBKV>(sK, p.k, 0, kend, col0);
-  load_tile<kBKV>(sV, p.v, 0, kend, col0);
-  cp_async_commit();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 9; ++i) mbar_init(&bars[i], i == 6 ? 4 : 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem;        // S (fp32) and, over its first 64 columns, P (bf16 pairs)
+  const uint32_t tO = tmem + 128;  // O accumulator
 
-  // the two query rows this thread holds: warp*16 + g and + 8
-  const int qg0 = p.q_off + r0 + warp * 16 + g;
-  const int qg1 = qg0 + 8;
-  const int lim0 = qg0 < p.L ? qg0 + 1 : p.Lk;  // keys [0, lim) are visible
-  const int lim1 = qg1 < p.L ? qg1 + 1 : p.Lk;
-
-  uint32_t qf[8][4];
-  float o[16][4];
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int k_last = -1, v_last = -1;  // last tile whose K / V load was issued
+      mbar_arrive_expect_tx(q_full, kTileBytes);
+      tma_load_2d(sQ, &tmQ, q_full, col0, r0);
+      tma_load_2d(sQ + kHalfBytes, &tmQ, q_full, col0 + 64, r0);
+      for (int j = 0; j < ntiles; ++j) {
+        if (*abort_flag) break;
+        const uint32_t par = j & 1;
+        if (!mbar_wait(k_empty, par ^ 1u)) {
+          report_error(p.err, kErrTimeoutProducer);
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(k_full, kTileBytes);
+        tma_load_2d(sK, &tmK, k_full, col0, j * kBKV);
+        tma_load_2d(sK + kHalfBytes, &tmK, k_full, col0 + 64, j * kBKV);
+        k_last = j;
+        if (!mbar_wait(v_empty, par ^ 1u)) {
+          report_error(p.err, kErrTimeoutProducer);
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(v_full, kTileBytes);
+        tma_load_2d(sV, &tmV, v_full, col0, j * kBKV);
+        tma_load_2d(sV + kHalfBytes, &tmV, v_full, col0 + 64, j * kBKV);
+        v_last = j;
+      }
+      // every load this thread issued must land before the CTA may exit
+      if (!mbar_wait(q_full, 0)) report_error(p.err, kErrTimeoutDrain);
+      if (k_last >= 0 && !mbar_wait(k_full, k_last & 1)) report_error(p.err, kErrTimeoutDrain);
+      if (v_last >= 0 && !mbar_wait(v_full, v_last & 1)) report_error(p.err, kErrTimeoutDrain);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      bool ok = mbar_wait(q_full, 0);
+      if (!ok) {
+        report_error(p.err, kErrTimeoutMma);
+        *abort_flag = 1;
+      }
+      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        if (*abort_flag) break;
+        const uint32_t par = j & 1;
+        // S may be overwritten once PV of the previous tile has read P
+        if (j > 0 && !mbar_wait(o_done, par ^ 1u)) ok = false;
+        if (ok && !mbar_wait(k_full, par)) ok = false;
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-  const int mi = lane >> 3;  // which 8x8 matrix this lane addresses in ldmatrix.x4
-  const int mr = lane & 7;
-
-  for (int kt = 0; kt < ntiles; ++kt) {
-    const int buf = kt & 1;
-    if (kt + 1 < ntiles) {
-      load_tile<kBKV>(sK + (buf ^ 1) * kTileKVBytes, p.k, (kt + 1) * kBKV, kend, col0);
-      load_tile<kBKV>(sV + (buf ^ 1) * kTileKVBytes, p.v, (kt + 1) * kBKV, kend, col0);
-      cp_async_commit();
-      cp_async_wait<1>();
+        for (int k = 0; k < kHeadDim / 16; ++k) {
+          const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
+          mma_bf16_ss(tS, sw128_kmajor_desc(q0 + off), sw128_kmajor_desc(k0 + off), kIdescQK, k > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full);
+        mma_commit(k_empty);
+        if (!mbar_wait(p_full, par) || !mbar_wait(v_full, par)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kBKV / 16; ++k) {
+          // P columns: 16 keys = 8 columns of bf16 pairs; V rows: 16 keys = 2 KB
+          mma_bf16_ts(tO, tS + k * 8, sw128_mnmajor_desc(v0 + k * 2048, kHalfBytes, 1024), kIdescPV,
+                      (j > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(o_done);
+        mma_commit(v_empty);
+      }
+      if (!ok) {
+        report_error(p.err, kErrTimeoutMma);
+        *abort_flag = 1;
+      }
+      mma_commit(drain);
+      if (!mbar_wait(drain, 0)) report_error(p.err, kErrTimeoutDrain);
+    }
+  } else {
+    // ---------------- softmax (warps 2..5), thread = one query row
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int row = r0 + row_in_tile;
+    const int qg = p.q_off + row;
+    const int lim = qg < p.L ? qg + 1 : p.Lk;  // keys [0, lim) are visible
+    float m_used = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const uint32_t par = j & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full, par));
+      if (!ok) break;
+      tc_fence_after();
+      const int kbase = j * kBKV;
+      // pass 1: the tile's row maximum (scaled to base 2)
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tS + lane_off + c * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float v = kbase + c * 32 + i < lim ? __uint_as_float(r[i]) * scale_log2 : -INFINITY;
+          mx = fmaxf(mx, v);
+        }
+      }
+      const float m_new = fmaxf(m_used, mx);
+      if (j == 0) {
+        m_used = m_new;
+      } else {
+        // O holds the sum over earlier tiles (their PV finished before this S was
+        // computed). A row whose maximum grew by more than 2^8 brings O and its
+        // row sum to the new maximum. tcgen05.ld/st must be executed by the whole
+        // warp, so the warp runs them if any row needs it; the other rows scale
+        // by exactly 1 and keep their maximum, so a row's result never depends
+        // on which rows share its warp.
+        const bool mine = m_new > m_used + kRescaleLog2;
+        if (__any_sync(0xffffffffu, mine)) {
+          const float alpha = mine ? fast_exp2(m_used - m_new) : 1.0f;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tO + lane_off + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(tO + lane_off + c * 32, r);
+          }
+          if (mine) {
+            l *= alpha;
+            m_used = m_new;
+          }
+        }
+      }
+      // pass 2: P = 2^(s - m) as bf16 pairs over the first 64 S columns
+      float rs = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tS + lane_off + c * 32, r);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int key = kbase + c * 32 + 2 * i;
+          const float a = key < lim ? fast_exp2(__uint_as_float(r[2 * i]) * scale_log2 - m_used) : 0.f;
+          const float b = key + 1 < lim ? fast_exp2(__uint_as_float(r[2 * i + 1]) * scale_log2 - m_used) : 0.f;
+          rs += a + b;
+          pk[i] = pack_bf16x2(a, b);
+        }
+        tmem_st16(tS + lane_off + c * 16, pk);
+      }
+      l += rs;
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    // epilogue: wait for the last PV, O / l -> bf16
+    if (ok && ntiles > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (ntiles - 1) & 1));
+    if (!ok) {
+      if (lane == 0) report_error(p.err, kErrTimeoutEpilogue);
+      *abort_flag = 1;
     } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-
-    if (kt == 0) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* dst = p.o + static_cast<size_t>(row) * kHidden + col0;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tO + lane_off + c * 32, r);
+        tmem_ld_wait();
+        if (row < p.Rq) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const int row = warp * 16 + (mi & 1) * 8 + mr;
-        const int col = kk * 16 + (mi >> 1) * 8;
-        ldsm_x4(sQ + swz(row, col), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+          for (int i = 0; i < 4; ++i) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv, __uint_as_float(r[8 * i + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv, __uint_as_float(r[8 * i + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv, __uint_as_float(r[8 * i + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv, __uint_as_float(r[8 * i + 7]) * inv);
+            d4[i] = w;
+          }
+        }
       }
     }
-
-    // S = Q K^T for 64 keys: 8 n-blocks of 8 keys
-    float s[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-    const uint32_t kb = sK + buf * kTileKVBytes;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-      for (int nb = 0; nb < 4; ++nb) {
-        const int key = nb * 16 + (mi >> 1) * 8 + mr;
-        const int col = kk * 16 + (mi & 1) * 8;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kb + swz(key, col), b0, b1, b2, b3);
-        mma16816(s[2 * nb], qf[kk], b0, b1);
-        mma16816(s[2 * nb + 1], qf[kk], b2, b3);
-      }
-    }
-
-    // scale, mask, online softmax (base 2)
-    const int kbase = kt * kBKV;
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int nb = 0; nb < 8; ++nb) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int key = kbase + nb * 8 + 2 * t4 + e;
-        float a = s[nb][e] * scale_log2;
-        float b = s[nb][2 + e] * scale_log2;
-        a = key < lim0 ? a : -INFINITY;
-        b = key < lim1 ? b : -INFINITY;
-        s[nb][e] = a;
-        s[nb][2 + e] = b;
-        mx0 = fmaxf(mx0, a);
-        mx1 = fmaxf(mx1, b);
-      }
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0);
-    const float mn1 = fmaxf(m1, mx1);
-    const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float alpha0 = exp2f(m0 - base0);
-    const float alpha1 = exp2f(m1 - base1);
-    m0 = mn0;
-    m1 = mn1;
-    float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-    for (int nb = 0; nb < 8; ++nb) {
-      s[nb][0] = exp2f(s[nb][0] - base0);
-      s[nb][1] = exp2f(s[nb][1] - base0);
-      s[nb][2] = exp2f(s[nb][2] - base1);
-      s[nb][3] = exp2f(s[nb][3] - base1);
-      rs0 += s[nb][0] + s[nb][1];
-      rs1 += s[nb][2] + s[nb][3];
-    }
-    l0 = l0 * alpha0 + rs0;
-    l1 = l1 * alpha1 + rs1;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      o[i][0] *= alpha0;
-      o[i][1] *= alpha0;
-      o[i][2] *= alpha1;
-      o[i][3] *= alpha1;
-    }
-
-    // O += P V: 4 k-steps of 16 keys, 16 n-blocks of 8 dims
-    const uint32_t vb = sV + buf * kTileKVBytes;
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      uint32_t pa[4];
-      pa[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
-      pa[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
-      pa[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      pa[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-#pragma unroll
-      for (int nd = 0; nd < 8; ++nd) {
-        const int key = kk * 16 + (mi & 1) * 8 + mr;
-        const int col = nd * 16 + (mi >> 1) * 8;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vb + swz(key, col), b0, b1, b2, b3);
-        mma16816(o[2 * nd], pa, b0, b1);
-        mma16816(o[2 * nd + 1], pa, b2, b3);
-      }
-    }
-    __syncthreads();
   }
 
-  // finish the row sums across the quad and write O
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
-  const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-  const int row0 = r0 + warp * 16 + g;
-  const int row1 = row0 + 8;
-#pragma unroll
-  for (int nd = 0; nd < 16; ++nd) {
-    const int col = col0 + nd * 8 + 2 * t4;
-    if (row0 < p.Rq)
-      *reinterpret_cast<uint32_t*>(p.o + static_cast<size_t>(row0) * kHidden + col) =
-          pack_bf16x2(o[nd][0] * inv0, o[nd][1] * inv0);
-    if (row1 < p.Rq)
-      *reinterpret_cast<uint32_t*>(p.o + static_cast<size_t>(row1) * kHidden + col) =
-          pack_bf16x2(o[nd][2] * inv1, o[nd][3] * inv1);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -253,13 +296,17 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
   if (p.Rq <= 0) return cudaSuccess;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kD));
+  CUtensorMap mq, mk, mv;
+  if (!encode_bf16_map(&mq, p.q, p.Rq, kHidden, 128) || !encode_bf16_map(&mk, p.k, p.Lk, kHidden, 128) ||
+      !encode_bf16_map(&mv, p.v, p.Lk, kHidden, 128))
+    return cudaErrorInvalidValue;
+  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kHeadDim));
   dim3 grid((p.Rq + kBQ - 1) / kBQ, kHeads);
-  attn_fwd<<<grid, kThreads, kSmem, stream>>>(p, scale_log2);
+  attn_tc<<<grid, 192, kSmem, stream>>>(mq, mk, mv, p, scale_log2);
   return cudaGetLastError();
 }
 

@@ -73,7 +73,12 @@ struct AttnParams {
   int q_off;
   int L;                   // text rows: global index < L
   int Lk;                  // keys visible to image rows
+  int* err;                // device error word (may be null)
 };
+
+// 2-D bf16 TMA map over a row-major [rows, cols] matrix, box = box_rows x 64
+// columns with 128-byte swizzle; rows past `rows` read as zero (qidit.cu).
+bool encode_bf16_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
 

@@ -75,18 +75,10 @@ EncodeTiledFn encode_fn() {
 // 2-D bf16 map over a row-major [rows, cols] matrix; box = box_rows x 64 columns
 // (one 128-byte swizzle span), rows past `rows` read as zero.
 qi_status make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return fail(QI_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  if (!encode_fn()) return fail(QI_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (cols * 2) % 16 != 0)
     return fail(QI_ERR_INVALID_ARG, "tensor map base or row pitch not 16-byte aligned");
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(QI_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  if (!qi::encode_bf16_map(m, base, rows, cols, box_rows)) return fail(QI_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   return QI_OK;
 }
 
@@ -245,6 +237,7 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
     a.q_off = q_off;
     a.L = L;
     a.Lk = Lk;
+    a.err = d->err;
     QI_CUDA(qi::launch_attention(a, s));
   }
   // out-projection: x += g1 * (o Wo^T); xa = bf16(x (1 + s2))
@@ -362,6 +355,18 @@ bool all_loaded(const qi_dit* d) {
 }  // namespace
 
 void qi::set_last_error(const char* msg) { g_last_error = msg; }
+
+bool qi::encode_bf16_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || (reinterpret_cast<uintptr_t>(base) & 15) != 0 || (cols * 2) % 16 != 0 || rows == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 // ================================================================ C ABI
 
