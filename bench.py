@@ -332,10 +332,11 @@ def run_ours(args, rank, world, local_rank):
     gu_ms, gu_n = prof["gateup_gemm"]
     gu_flops = BLOCKS * (njoint * gateup_flops(True) + nimg * gateup_flops(False))
     gu_tflops = gu_flops / (gu_ms / 1e3) / 1e12 if gu_ms > 0 else None
+    # dram read + write bytes per gate/up launch from the last ncu capture of this kernel
     traffic = None
     try:
-        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            traffic = json.load(f).get("gateup_gemm_bytes_per_launch")
+        with open(os.path.join(ROOT, "profiles", "traffic_gateup_gemm.txt")) as f:
+            traffic = float(f.read().split()[0])
     except Exception:
         pass
 

@@ -187,19 +187,26 @@ __global__ void __launch_bounds__(192, 2)
       if (!ok) break;
       tc_fence_after();
       const int kbase = j * kBKV;
-      // pass 1: the tile's row maximum (scaled to base 2)
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tS + lane_off + c * 32, r);
-        tmem_ld_wait();
+      // the whole S row of this tile: four loads in flight, one wait
+      uint32_t r[4][32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float v = kbase + c * 32 + i < lim ? __uint_as_float(r[i]) * scale_log2 : -INFINITY;
-          mx = fmaxf(mx, v);
-        }
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, r[c]);
+      tmem_ld_wait();
+      // keys at or past the row's limit become -inf (only tiles that reach a limit)
+      if (__any_sync(0xffffffffu, kbase + kBKV > lim)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (kbase + c * 32 + i >= lim) r[c][i] = 0xff800000u;
       }
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(r[c][i]));
+      // the tile's row maximum in base-2 units (scale > 0 keeps the order)
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
       const float m_new = fmaxf(m_used, mx);
       if (j == 0) {
         m_used = m_new;
@@ -214,13 +221,13 @@ __global__ void __launch_bounds__(192, 2)
         if (__any_sync(0xffffffffu, mine)) {
           const float alpha = mine ? fast_exp2(m_used - m_new) : 1.0f;
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tO + lane_off + c * 32, r);
+          for (int c = 0; c < 8; ++c) {
+            uint32_t o[16];
+            tmem_ld16(tO + lane_off + c * 16, o);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(tO + lane_off + c * 32, r);
+            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st16(tO + lane_off + c * 16, o);
           }
           if (mine) {
             l *= alpha;
@@ -228,25 +235,22 @@ __global__ void __launch_bounds__(192, 2)
           }
         }
       }
-      // pass 2: P = 2^(s - m) as bf16 pairs over the first 64 S columns
-      float rs = 0.f;
-#pragma unroll 1
+      // P = 2^(s * scale - m) as bf16 pairs over the first 64 S columns (masked
+      // keys give 2^-inf = 0). Chunk c of P covers S columns already read.
+      float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tS + lane_off + c * 32, r);
-        tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int key = kbase + c * 32 + 2 * i;
-          const float a = key < lim ? fast_exp2(__uint_as_float(r[2 * i]) * scale_log2 - m_used) : 0.f;
-          const float b = key + 1 < lim ? fast_exp2(__uint_as_float(r[2 * i + 1]) * scale_log2 - m_used) : 0.f;
-          rs += a + b;
+          const float a = fast_exp2(fmaf(__uint_as_float(r[c][2 * i]), scale_log2, -m_used));
+          const float b = fast_exp2(fmaf(__uint_as_float(r[c][2 * i + 1]), scale_log2, -m_used));
+          rs4[i & 3] += a + b;
           pk[i] = pack_bf16x2(a, b);
         }
         tmem_st16(tS + lane_off + c * 16, pk);
       }
-      l += rs;
+      l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();

@@ -26,7 +26,8 @@ constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;  // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
+constexpr int kEpiScratch = 4 * 32 * 33 * 4;  // per epilogue warp: one 32 x 32 fp32 chunk, stride 33
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256 + kEpiScratch;
 constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
 constexpr uint32_t kTmemCols = 512;  // two 256-column accumulators
 constexpr int kGroupN = 8;           // tiles sweep 8 column tiles per row tile for L2 reuse
@@ -120,55 +121,64 @@ __device__ __forceinline__ void epi_qkv(const GemmParams& p, uint32_t taddr, int
   }
 }
 
-__device__ __forceinline__ void epi_resid(const GemmParams& p, uint32_t taddr, int row, int n0) {
-  const bool valid = row < p.M;
-  const float* mrow = p.mod + (row < p.n_text ? kMod : 0);
-  const float* gate = mrow + p.gate_chunk * kHidden + n0;
-  const float* scale = mrow + p.scale_chunk * kHidden + n0;
-  float* xrow = p.x + static_cast<size_t>(row) * kHidden + n0;
-  __nv_bfloat16* arow = p.xa + static_cast<size_t>(row) * kHidden + n0;
-  float ss = 0.f;
+// Residual epilogue. The accumulator arrives one row per lane; each 32 x 32
+// chunk is transposed through shared memory (stride 33: conflict-free both
+// ways) so that lane i handles column i of the warp's 32 rows and every global
+// access of the fp32 residual and the bf16 copy is one contiguous row segment.
+// Per row: x = acc + bias (set) or x += gate * acc; xa = bf16(x * (1 + scale));
+// the row's sum of squares over the tile's 256 columns is accumulated per lane
+// and reduced per row in a fixed order.
+__device__ __forceinline__ void epi_resid(const GemmParams& p, uint32_t taddr, int row0, int lane, int n0,
+                                          float* sm) {
+  float sq[32];
+#pragma unroll
+  for (int rr = 0; rr < 32; ++rr) sq[rr] = 0.f;
 #pragma unroll 1
   for (int c = 0; c < kBN / 32; ++c) {
     uint32_t r[32];
     tmem_ld32(taddr + c * 32, r);
     tmem_ld_wait();
-    if (!valid) continue;
-    float xn[32], av[32];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int col = c * 32 + 4 * i;
-      float4 base;
-      if (p.resid_set) {
-        const uint2 bb = *reinterpret_cast<const uint2*>(p.bias + n0 + col);
-        base.x = __uint_as_float(bb.x << 16);
-        base.y = __uint_as_float(bb.x & 0xFFFF0000u);
-        base.z = __uint_as_float(bb.y << 16);
-        base.w = __uint_as_float(bb.y & 0xFFFF0000u);
-        xn[4 * i + 0] = __uint_as_float(r[4 * i + 0]) + base.x;
-        xn[4 * i + 1] = __uint_as_float(r[4 * i + 1]) + base.y;
-        xn[4 * i + 2] = __uint_as_float(r[4 * i + 2]) + base.z;
-        xn[4 * i + 3] = __uint_as_float(r[4 * i + 3]) + base.w;
-      } else {
-        base = *reinterpret_cast<const float4*>(xrow + col);
-        const float4 g = *reinterpret_cast<const float4*>(gate + col);
-        xn[4 * i + 0] = base.x + g.x * __uint_as_float(r[4 * i + 0]);
-        xn[4 * i + 1] = base.y + g.y * __uint_as_float(r[4 * i + 1]);
-        xn[4 * i + 2] = base.z + g.z * __uint_as_float(r[4 * i + 2]);
-        xn[4 * i + 3] = base.w + g.w * __uint_as_float(r[4 * i + 3]);
+    for (int k = 0; k < 32; ++k) sm[lane * 33 + k] = __uint_as_float(r[k]);
+    __syncwarp();
+    float acc[32];
+#pragma unroll
+    for (int rr = 0; rr < 32; ++rr) acc[rr] = sm[rr * 33 + lane];
+    __syncwarp();
+    const int col = n0 + c * 32 + lane;
+    const float g_img = p.mod[p.gate_chunk * kHidden + col];
+    const float g_txt = p.mod[kMod + p.gate_chunk * kHidden + col];
+    const float s_img = 1.f + p.mod[p.scale_chunk * kHidden + col];
+    const float s_txt = 1.f + p.mod[kMod + p.scale_chunk * kHidden + col];
+    const float bias = p.resid_set ? bf16_bits_to_float(p.bias[col]) : 0.f;
+    // all 32 residual loads in flight before any store (the stores could alias
+    // them as far as the compiler knows, which would serialise the rows)
+    float xo[32];
+    const float* xcol = p.x + static_cast<size_t>(row0) * kHidden + col;
+#pragma unroll
+    for (int rr = 0; rr < 32; ++rr)
+      xo[rr] = (!p.resid_set && row0 + rr < p.M) ? xcol[static_cast<size_t>(rr) * kHidden] : 0.f;
+#pragma unroll
+    for (int rr = 0; rr < 32; ++rr) {
+      const int row = row0 + rr;
+      if (row < p.M) {
+        const bool txt = row < p.n_text;
+        const size_t idx = static_cast<size_t>(row) * kHidden + col;
+        const float xn = p.resid_set ? acc[rr] + bias : xo[rr] + (txt ? g_txt : g_img) * acc[rr];
+        p.x[idx] = xn;
+        sq[rr] += xn * xn;
+        p.xa[idx] = __float2bfloat16_rn(xn * (txt ? s_txt : s_img));
       }
-      *reinterpret_cast<float4*>(xrow + col) = make_float4(xn[4 * i], xn[4 * i + 1], xn[4 * i + 2], xn[4 * i + 3]);
-      const float4 s = *reinterpret_cast<const float4*>(scale + col);
-      av[4 * i + 0] = xn[4 * i + 0] * (1.f + s.x);
-      av[4 * i + 1] = xn[4 * i + 1] * (1.f + s.y);
-      av[4 * i + 2] = xn[4 * i + 2] * (1.f + s.z);
-      av[4 * i + 3] = xn[4 * i + 3] * (1.f + s.w);
     }
-#pragma unroll
-    for (int i = 0; i < 32; ++i) ss += xn[i] * xn[i];
-    store_bf16x32(arow + c * 32, av);
   }
-  if (valid) p.ssp_out[static_cast<size_t>(row) * kSspParts + n0 / kBN] = ss;
+#pragma unroll
+  for (int rr = 0; rr < 32; ++rr) sm[rr * 33 + lane] = sq[rr];
+  __syncwarp();
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) ss += sm[lane * 33 + k];
+  __syncwarp();
+  if (row0 + lane < p.M) p.ssp_out[static_cast<size_t>(row0 + lane) * kSspParts + n0 / kBN] = ss;
 }
 
 __device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, int row, int n0) {
@@ -359,7 +369,8 @@ __global__ void __launch_bounds__(192, 1)
       if (KIND == kEpiQkv)
         epi_qkv(p, taddr, row, nt * kBN);
       else if (KIND == kEpiResid)
-        epi_resid(p, taddr, row, nt * kBN);
+        epi_resid(p, taddr, mt * kBM + quarter * 32, lane, nt * kBN,
+                  reinterpret_cast<float*>(smem + kStages * kStageBytes + 256) + (warp - 2) * 32 * 33);
       else if (KIND == kEpiSwiglu)
         epi_swiglu(p, taddr, row, nt * kBN);
       else
