@@ -351,11 +351,13 @@ def run_ours(args, rank, world, local_rank):
                    "joint_steps": njoint, "image_only_steps": nimg},
         "achieved_tflops": tflops,
         "tflops_frac_of_peak": tflops / world / peak_b,
+        "tflops_frac_of_sustained_peak": tflops / world / peak_s,
         "gpu_launches": njoint * launches_per_step(True) + nimg * launches_per_step(False),
         "roofline": {"kernel": "gate/up GEMM + SwiGLU epilogue (tcgen05)", "bound": "tensor",
-                     "achieved": gu_tflops, "peak": peak_b, "unit": "TFLOP/s",
-                     "frac": (gu_tflops / peak_b) if gu_tflops else None, "traffic": traffic,
-                     "peak_kind": f"{peak_kind} bf16 burst", "launches": gu_n,
+                     "achieved": gu_tflops, "peak": peak_s, "unit": "TFLOP/s",
+                     "frac": (gu_tflops / peak_s) if gu_tflops else None, "traffic": traffic,
+                     "peak_kind": f"{peak_kind} bf16 sustained (the kernel runs inside a seconds-long loop)",
+                     "frac_of_burst": (gu_tflops / peak_b) if gu_tflops else None, "launches": gu_n,
                      "avg_launch_ms": gu_ms / gu_n if gu_n else None},
         "kernel_ms": {k: v[0] for k, v in prof.items()},
         "e2e": {"value": world * e2e_steps / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": h2d / e2e_steps,
