@@ -29,7 +29,7 @@ PROF_CLASSES = ("qkv_gemm", "attention", "out_gemm", "gateup_gemm", "down_gemm",
 
 STATUS = {
     0: "QI_OK", 1: "QI_ERR_INVALID_ARG", 2: "QI_ERR_SHAPE", 3: "QI_ERR_STATE", 4: "QI_ERR_OOM",
-    5: "QI_ERR_CUDA", 6: "QI_ERR_DEVICE_TIMEOUT", 7: "QI_ERR_NOT_IMPLEMENTED",
+    5: "QI_ERR_CUDA", 6: "QI_ERR_DEVICE_TIMEOUT", 7: "QI_ERR_NOT_IMPLEMENTED", 8: "QI_ERR_NONFINITE",
 }
 
 # every symbol include/qidit.h declares
@@ -38,7 +38,7 @@ SYMBOLS = (
     "qi_rope_axis_tables", "qi_rope_tables", "qi_flow_sigmas", "qi_pack_noise", "qi_euler_update",
     "qi_dit_step", "qi_text_kv_capture", "qi_kv_cache_bytes", "qi_dit_check",
     "qi_dit_block_forward", "qi_dit_read_kv", "qi_dit_set_trace", "qi_dit_profile",
-    "qi_dit_profile_read", "qi_last_error", "qi_gemm_bf16", "qi_attention_bf16", "qi_gemm_bf16_noalloc",
+    "qi_dit_profile_read", "qi_last_error", "qi_gemm_bf16", "qi_attention_f16", "qi_gemm_bf16_noalloc",
 )
 
 
@@ -102,7 +102,7 @@ def lib() -> ctypes.CDLL:
         "qi_dit_profile": [P, I],
         "qi_dit_profile_read": [P, P, P],
         "qi_gemm_bf16": [P, P, P, P, I, I, I, P],
-        "qi_attention_bf16": [P, P, P, P, I, I, I, I, P],
+        "qi_attention_f16": [P, P, P, P, I, I, I, I, P],
         "qi_gemm_bf16_noalloc": [P, P, P, I, I, I, I, P],
     }
     for name, args in sig.items():
@@ -201,12 +201,12 @@ def euler_update(x, vel, sigma_i: float, sigma_next: float):
 
 
 def attention(q, k, v, L: int, q_off: int = 0, Lk: int | None = None):
-    """Test hook: block-causal attention, bf16 q [Rq, 4096], k/v [Lk, 4096] -> o [Rq, 4096]."""
+    """Test hook: block-causal attention, fp16 q [Rq, 4096], k/v [Lk, 4096] -> o [Rq, 4096]."""
     import torch
     Rq = q.shape[0]
     Lk = k.shape[0] if Lk is None else Lk
     o = torch.empty(Rq, HIDDEN, dtype=q.dtype, device=q.device)
-    _check(lib().qi_attention_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(o), Rq, q_off, L, Lk, _stream()))
+    _check(lib().qi_attention_f16(_ptr(q), _ptr(k), _ptr(v), _ptr(o), Rq, q_off, L, Lk, _stream()))
     return o
 
 
@@ -325,7 +325,7 @@ class DiT:
         return hidden
 
     def read_kv(self, b: int, row0: int, rows: int):
-        """(K, V) int16-viewed bf16 bits [rows, 4096] of block b (device copies)."""
+        """(K, V) int16-viewed fp16 bits [rows, 4096] of block b (device copies)."""
         import torch
         k = torch.empty(rows, HIDDEN, dtype=torch.int16, device=f"cuda:{self.device}")
         v = torch.empty_like(k)

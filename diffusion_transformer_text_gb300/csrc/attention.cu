@@ -17,7 +17,7 @@
 //   warps 2-5  softmax: thread = query row (TMEM lane). Reads its S row, keeps a
 //              running max (O is rescaled only when the max grows by more than
 //              2^8, the row sum uses the same max, so the result is unchanged),
-//              writes P as bf16 over the S columns, and at the end scales O by
+//              writes P as fp16 over the S columns, and at the end scales O by
 //              1 / rowsum and stores it.
 // Every mbarrier wait is bounded; on expiry the error word is set and the CTA
 // drains its copies and MMAs before releasing TMEM.
@@ -33,8 +33,8 @@ constexpr int kHalfBytes = 128 * 64 * 2;       // one 128-row x 64-column swizzl
 constexpr int kTileBytes = 2 * kHalfBytes;     // 128 rows x 128 dims: 32 KB
 constexpr int kSmem = 3 * kTileBytes + 1024 + 256;
 constexpr uint32_t kTmemCols = 256;            // S/P: columns [0,128), O: [128,256)
-constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128);
-constexpr uint32_t kIdescPV = idesc_bf16_f32_bmn(128, 128);
+constexpr uint32_t kIdescQK = idesc_f16_f32(128, 128);
+constexpr uint32_t kIdescPV = idesc_f16_f32_bmn(128, 128);
 constexpr float kRescaleLog2 = 8.0f;           // rescale O only when the max grows by > 2^8
 
 __global__ void __launch_bounds__(192, 2)
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(192, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;        // S (fp32) and, over its first 64 columns, P (bf16 pairs)
+  const uint32_t tS = tmem;        // S (fp32) and, over its first 64 columns, P (fp16 pairs)
   const uint32_t tO = tmem + 128;  // O accumulator
 
   if (warp == 0) {
@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(192, 2)
 #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k) {
           const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-          mma_bf16_ss(tS, sw128_kmajor_desc(q0 + off), sw128_kmajor_desc(k0 + off), kIdescQK, k > 0 ? 1u : 0u);
+          mma_ss(tS, sw128_kmajor_desc(q0 + off), sw128_kmajor_desc(k0 + off), kIdescQK, k > 0 ? 1u : 0u);
         }
         mma_commit(s_full);
         mma_commit(k_empty);
@@ -156,8 +156,8 @@ __global__ void __launch_bounds__(192, 2)
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < kBKV / 16; ++k) {
-          // P columns: 16 keys = 8 columns of bf16 pairs; V rows: 16 keys = 2 KB
-          mma_bf16_ts(tO, tS + k * 8, sw128_mnmajor_desc(v0 + k * 2048, kHalfBytes, 1024), kIdescPV,
+          // P columns: 16 keys = 8 columns of fp16 pairs; V rows: 16 keys = 2 KB
+          mma_ts(tO, tS + k * 8, sw128_mnmajor_desc(v0 + k * 2048, kHalfBytes, 1024), kIdescPV,
                       (j > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(o_done);
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(192, 2)
           }
         }
       }
-      // P = 2^(s * scale - m) as bf16 pairs over the first 64 S columns (masked
+      // P = 2^(s * scale - m) as fp16 pairs over the first 64 S columns (masked
       // keys give 2^-inf = 0). Chunk c of P covers S columns already read.
       float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(192, 2)
           const float a = fast_exp2(fmaf(__uint_as_float(r[c][2 * i]), scale_log2, -m_used));
           const float b = fast_exp2(fmaf(__uint_as_float(r[c][2 * i + 1]), scale_log2, -m_used));
           rs4[i & 3] += a + b;
-          pk[i] = pack_bf16x2(a, b);
+          pk[i] = pack_f16x2(a, b);
         }
         tmem_st16(tS + lane_off + c * 16, pk);
       }
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(192, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    // epilogue: wait for the last PV, O / l -> bf16
+    // epilogue: wait for the last PV, O / l -> fp16
     if (ok && ntiles > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (ntiles - 1) & 1));
     if (!ok) {
       if (lane == 0) report_error(p.err, kErrTimeoutEpilogue);
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(192, 2)
     } else {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* dst = p.o + static_cast<size_t>(row) * kHidden + col0;
+      act_t* dst = p.o + static_cast<size_t>(row) * kHidden + col0;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
@@ -275,10 +275,10 @@ __global__ void __launch_bounds__(192, 2)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv, __uint_as_float(r[8 * i + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv, __uint_as_float(r[8 * i + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv, __uint_as_float(r[8 * i + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv, __uint_as_float(r[8 * i + 7]) * inv);
+            w.x = pack_f16x2(__uint_as_float(r[8 * i + 0]) * inv, __uint_as_float(r[8 * i + 1]) * inv);
+            w.y = pack_f16x2(__uint_as_float(r[8 * i + 2]) * inv, __uint_as_float(r[8 * i + 3]) * inv);
+            w.z = pack_f16x2(__uint_as_float(r[8 * i + 4]) * inv, __uint_as_float(r[8 * i + 5]) * inv);
+            w.w = pack_f16x2(__uint_as_float(r[8 * i + 6]) * inv, __uint_as_float(r[8 * i + 7]) * inv);
             d4[i] = w;
           }
         }
@@ -305,8 +305,8 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
     attr_set = true;
   }
   CUtensorMap mq, mk, mv;
-  if (!encode_bf16_map(&mq, p.q, p.Rq, kHidden, 128) || !encode_bf16_map(&mk, p.k, p.Lk, kHidden, 128) ||
-      !encode_bf16_map(&mv, p.v, p.Lk, kHidden, 128))
+  if (!encode_map16(&mq, p.q, p.Rq, kHidden, 128, false) || !encode_map16(&mk, p.k, p.Lk, kHidden, 128, false) ||
+      !encode_map16(&mv, p.v, p.Lk, kHidden, 128, false))
     return cudaErrorInvalidValue;
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kHeadDim));
   dim3 grid((p.Rq + kBQ - 1) / kBQ, kHeads);

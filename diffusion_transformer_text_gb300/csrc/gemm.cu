@@ -2,8 +2,9 @@
 // contractions (QKV, out-projection, SwiGLU gate/up, down, text projection),
 // with the block's elementwise work fused into the epilogue.
 //
-// D[M, N] = A[M, K] * B[N, K]^T; A = bf16 activations, B = bf16 weights
-// ([out, in] row-major), fp32 accumulation in tensor memory.
+// D[M, N] = A[M, K] * B[N, K]^T; A = fp16 activations, B = fp16 weights (converted
+// from the bf16 checkpoint values; [out, in] row-major), fp32 accumulation in
+// tensor memory. The plain fp32 epilogue (a test hook) takes bf16 operands.
 //
 // Roles per CTA (192 threads):
 //   warp 0     TMA producer: 128x64 A and 256x64 B tiles into a 4-stage ring
@@ -28,7 +29,9 @@ constexpr int kBBytes = kBN * kBK * 2;  // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kEpiScratch = 4 * 32 * 33 * 4;  // per epilogue warp: one 32 x 32 fp32 chunk, stride 33
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256 + kEpiScratch;
-constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
+// fp16 operands for the DiT epilogues, bf16 for the plain fp32 test hook
+template <int KIND>
+constexpr uint32_t kIdesc = KIND == kEpiF32 ? idesc_bf16_f32(kBM, kBN) : idesc_f16_f32(kBM, kBN);
 constexpr uint32_t kTmemCols = 512;  // two 256-column accumulators
 constexpr int kGroupN = 8;           // tiles sweep 8 column tiles per row tile for L2 reuse
 
@@ -56,15 +59,15 @@ __device__ __forceinline__ float row_rinv(const float* ssp, int row) {
   return rsqrtf(s * (1.0f / kHidden) + kEps);
 }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&v)[32]) {
+__device__ __forceinline__ void store_f16x32(act_t* dst, const float (&v)[32]) {
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     uint4 w;
-    w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
-    w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
-    w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
-    w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+    w.x = pack_f16x2(v[8 * i + 0], v[8 * i + 1]);
+    w.y = pack_f16x2(v[8 * i + 2], v[8 * i + 3]);
+    w.z = pack_f16x2(v[8 * i + 4], v[8 * i + 5]);
+    w.w = pack_f16x2(v[8 * i + 6], v[8 * i + 7]);
     d[i] = w;
   }
 }
@@ -76,7 +79,7 @@ __device__ __forceinline__ void epi_qkv(const GemmParams& p, uint32_t taddr, int
   float rinv = 0.f;
   const float* cs = nullptr;
   const float* sn = nullptr;
-  __nv_bfloat16* dst = nullptr;
+  act_t* dst = nullptr;
   const int section = n0 / kHidden;  // 0 Q, 1 K, 2 V
   const int col_in = n0 - section * kHidden;
   if (valid) {
@@ -117,15 +120,15 @@ __device__ __forceinline__ void epi_qkv(const GemmParams& p, uint32_t taddr, int
         v[2 * j + 1] = a * sv[j] + b * cv[j];
       }
     }
-    store_bf16x32(dst + c * 32, v);
+    store_f16x32(dst + c * 32, v);
   }
 }
 
 // Residual epilogue. The accumulator arrives one row per lane; each 32 x 32
 // chunk is transposed through shared memory (stride 33: conflict-free both
 // ways) so that lane i handles column i of the warp's 32 rows and every global
-// access of the fp32 residual and the bf16 copy is one contiguous row segment.
-// Per row: x = acc + bias (set) or x += gate * acc; xa = bf16(x * (1 + scale));
+// access of the fp32 residual and the fp16 copy is one contiguous row segment.
+// Per row: x = acc + bias (set) or x += gate * acc; xa = fp16(x * (1 + scale));
 // the row's sum of squares over the tile's 256 columns is accumulated per lane
 // and reduced per row in a fixed order.
 __device__ __forceinline__ void epi_resid(const GemmParams& p, uint32_t taddr, int row0, int lane, int n0,
@@ -167,7 +170,7 @@ __device__ __forceinline__ void epi_resid(const GemmParams& p, uint32_t taddr, i
         const float xn = p.resid_set ? acc[rr] + bias : xo[rr] + (txt ? g_txt : g_img) * acc[rr];
         p.x[idx] = xn;
         sq[rr] += xn * xn;
-        p.xa[idx] = __float2bfloat16_rn(xn * (txt ? s_txt : s_img));
+        p.xa[idx] = __float2half_rn(xn * (txt ? s_txt : s_img));
       }
     }
   }
@@ -185,7 +188,7 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, 
   const bool valid = row < p.M;
   const float rinv = valid ? row_rinv(p.ssp_in, row) : 0.f;
   // tile columns [0,128) are gate rows 128j.., [128,256) the matching up rows
-  __nv_bfloat16* dst = p.h + static_cast<size_t>(row) * kFfn + (n0 / kBN) * (kBN / 2);
+  act_t* dst = p.h + static_cast<size_t>(row) * kFfn + (n0 / kBN) * (kBN / 2);
 #pragma unroll 1
   for (int c = 0; c < kBN / 64; ++c) {
     uint32_t g[32], u[32];
@@ -200,7 +203,7 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, 
       const float b = __uint_as_float(u[i]) * rinv;
       hv[i] = a / (1.f + __expf(-a)) * b;
     }
-    store_bf16x32(dst + c * 32, hv);
+    store_f16x32(dst + c * 32, hv);
   }
 }
 
@@ -331,7 +334,7 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t b0 = smem_u32(sB + stage * kBBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            mma_bf16_ss(d, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k), kIdesc,
+            mma_ss(d, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k), kIdesc<KIND>,
                         (kb | k) != 0 ? 1u : 0u);
           mma_commit(&empty[stage]);
           if (++stage == kStages) {

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -17,18 +18,36 @@ constexpr int kTdim = 256;
 constexpr int kRopeCols = 64;
 constexpr float kEps = 1e-6f;
 
+// Codes a kernel writes into the device error word (first error wins).
+enum DeviceError : int {
+  kErrNone = 0,
+  kErrTimeoutProducer = 1,  // a bounded mbarrier wait expired in a TMA producer
+  kErrTimeoutMma = 2,       // ... in an MMA issuer
+  kErrTimeoutEpilogue = 3,  // ... in an epilogue / softmax warp
+  kErrTimeoutDrain = 4,     // ... while draining copies or MMAs before exit
+  kErrNonFinite = 5,        // the output head produced a non-finite velocity
+};
+
+// Tensor-core operands of the DiT pass (GEMM A and B, Q/K/V, P, O) are fp16:
+// the bf16 weights convert to fp16 exactly (except values below 2^-14, which
+// lose < 2^-25), and fp16's 11-bit significand keeps the rounding of the
+// activations 8x smaller than bf16's at the same tensor-core rate.
+// Accumulation is fp32 throughout; the residual stream is fp32.
+using act_t = __half;
+
 // GEMM tile: 128 rows x 256 columns per CTA, K in steps of 64 (one 128-byte
-// swizzle span of bf16). Sum-of-squares partials are kept per 256-column tile.
+// swizzle span of 16-bit elements). Sum-of-squares partials are kept per
+// 256-column tile.
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
 constexpr int kSspParts = kHidden / kBN;  // 16 partial sums per row
 
 enum EpiKind : int {
-  kEpiQkv = 0,     // row scale 1/rms, RoPE on Q and K, bf16 Q / K / V stores
-  kEpiResid = 1,   // residual update (+ gate) or bias set, bf16 modulated copy, sum of squares
-  kEpiSwiglu = 2,  // row scale 1/rms, silu(gate) * up, bf16 store
-  kEpiF32 = 3,     // plain fp32 store of D (test hook)
+  kEpiQkv = 0,     // row scale 1/rms, RoPE on Q and K, fp16 Q / K / V stores
+  kEpiResid = 1,   // residual update (+ gate) or bias set, fp16 modulated copy, sum of squares
+  kEpiSwiglu = 2,  // row scale 1/rms, silu(gate) * up, fp16 store
+  kEpiF32 = 3,     // plain fp32 store of D (test hooks, bf16 operands)
 };
 
 struct GemmParams {
@@ -37,21 +56,21 @@ struct GemmParams {
   const float* mod;    // [2][kMod]: row 0 for the sampled t, row 1 for t = 0
   const float* ssp_in; // [M][kSspParts] sum-of-squares partials of the GEMM's A rows
   // kEpiQkv
-  __nv_bfloat16* q;
-  __nv_bfloat16* k;
-  __nv_bfloat16* v;
+  act_t* q;
+  act_t* k;
+  act_t* v;
   int kv_row_off;      // K/V store row = activation row + kv_row_off
   const float* txt_cos;
   const float* txt_sin;
   const float* img_cos;
   const float* img_sin;
   // kEpiSwiglu
-  __nv_bfloat16* h;
+  act_t* h;
   // kEpiResid
   float* x;                 // fp32 residual stream [M][kHidden]
-  __nv_bfloat16* xa;        // bf16(x * (1 + scale)) for the next GEMM
+  act_t* xa;                // fp16(x * (1 + scale)) for the next GEMM
   float* ssp_out;           // [M][kSspParts]
-  const uint16_t* bias;     // set mode: x = acc + bias
+  const uint16_t* bias;     // set mode: x = acc + bias (bf16 bits)
   int resid_set;            // 1: x = acc + bias; 0: x += gate * acc
   int gate_chunk;           // modulation chunk used as gate (0..3)
   int scale_chunk;          // modulation chunk used as (1 + scale) for xa
@@ -60,38 +79,39 @@ struct GemmParams {
 };
 
 // Launch one persistent tcgen05 GEMM D[M,N] = A[M,K] * B[N,K]^T with the
-// epilogue `kind`. A and B maps are 2-D bf16 maps with box {64, 128} / {64, 256}.
+// epilogue `kind`. A and B maps are 2-D 16-bit maps with box {64, 128} /
+// {64, 256}; the operands are fp16 for the DiT epilogues and bf16 for kEpiF32.
 cudaError_t launch_gemm(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                         int grid_ctas, cudaStream_t stream);
 
 struct AttnParams {
-  const __nv_bfloat16* q;  // [Rq][kHidden], query row r has global index r + q_off
-  const __nv_bfloat16* k;  // [Lk][kHidden], key rows 0..Lk-1 (text first)
-  const __nv_bfloat16* v;
-  __nv_bfloat16* o;        // [Rq][kHidden]
+  const act_t* q;  // [Rq][kHidden], query row r has global index r + q_off
+  const act_t* k;  // [Lk][kHidden], key rows 0..Lk-1 (text first)
+  const act_t* v;
+  act_t* o;        // [Rq][kHidden]
   int Rq;
   int q_off;
-  int L;                   // text rows: global index < L
-  int Lk;                  // keys visible to image rows
-  int* err;                // device error word (may be null)
+  int L;           // text rows: global index < L
+  int Lk;          // keys visible to image rows
+  int* err;        // device error word (may be null)
 };
 
-// 2-D bf16 TMA map over a row-major [rows, cols] matrix, box = box_rows x 64
-// columns with 128-byte swizzle; rows past `rows` read as zero (qidit.cu).
-bool encode_bf16_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
-
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
+
+// 2-D 16-bit TMA map over a row-major [rows, cols] matrix, box = box_rows x 64
+// columns with 128-byte swizzle; rows past `rows` read as zero (qidit.cu).
+bool encode_map16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows, bool bf16);
 
 // Small kernels (kernels_small.cu)
 cudaError_t launch_timestep_embed(float t, float* e, cudaStream_t s);
 cudaError_t launch_gemv2(const float* x, int in_dim, const uint16_t* W, const uint16_t* b, int out_dim, float* y,
                          int silu_in, cudaStream_t s);
-cudaError_t launch_txt_prenorm(const float* txt, int L, const uint16_t* w, __nv_bfloat16* out, cudaStream_t s);
+cudaError_t launch_txt_prenorm(const float* txt, int L, const uint16_t* w, act_t* out, cudaStream_t s);
 cudaError_t launch_img_in(const float* img, int N, const uint16_t* W, const uint16_t* b, const float* mod,
-                          float* x, __nv_bfloat16* xa, float* ssp, cudaStream_t s);
+                          float* x, act_t* xa, float* ssp, cudaStream_t s);
 cudaError_t launch_head(const float* x, int N, const float* ssp, const uint16_t* W, const uint16_t* b, float* vel,
-                        cudaStream_t s);
-cudaError_t launch_block_prep(const float* x, int R, int n_text, const float* mod, __nv_bfloat16* xa, float* ssp,
+                        int* err, cudaStream_t s);
+cudaError_t launch_block_prep(const float* x, int R, int n_text, const float* mod, act_t* xa, float* ssp,
                               cudaStream_t s);
 cudaError_t launch_euler(float* x, const float* vel, long long n, float s_i, float s_next, cudaStream_t s);
 cudaError_t launch_rope_axis(float theta, float* c0, float* s0, float* c1, float* s1, float* c2, float* s2,
@@ -99,6 +119,9 @@ cudaError_t launch_rope_axis(float theta, float* c0, float* s0, float* c1, float
 cudaError_t launch_rope_tokens(int L, int h, int w, float theta, float* tc, float* ts, float* ic, float* is,
                                cudaStream_t s);
 cudaError_t launch_pack_noise(const float* z, int h, int w, float* x, cudaStream_t s);
+// In place bf16 -> fp16 for a weight tensor of n elements; values whose
+// magnitude exceeds the fp16 range are counted into *overflow.
+cudaError_t launch_bf16_to_f16(uint16_t* w, size_t n, unsigned int* overflow, cudaStream_t s);
 
 // Sets the calling thread's message returned by qi_last_error() (qidit.cu).
 void set_last_error(const char* msg);

@@ -89,10 +89,10 @@ __device__ __forceinline__ float block_sum_256(float v, float* red) {
   return s;
 }
 
-// ZeroCenterRMSNorm of text features: out = bf16(x / rms(x) * (1 + w)).
+// ZeroCenterRMSNorm of text features: out = fp16(x / rms(x) * (1 + w)).
 __global__ void __launch_bounds__(256) txt_prenorm_kernel(const float* __restrict__ txt,
                                                           const uint16_t* __restrict__ w,
-                                                          __nv_bfloat16* __restrict__ out) {
+                                                          act_t* __restrict__ out) {
   __shared__ float red[8];
   const int row = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(txt + static_cast<size_t>(row) * kHidden);
@@ -111,17 +111,17 @@ __global__ void __launch_bounds__(256) txt_prenorm_kernel(const float* __restric
     const float g0 = 1.f + __uint_as_float(wb.x << 16), g1 = 1.f + __uint_as_float(wb.x & 0xFFFF0000u);
     const float g2 = 1.f + __uint_as_float(wb.y << 16), g3 = 1.f + __uint_as_float(wb.y & 0xFFFF0000u);
     uint2 o;
-    o.x = pack_bf16x2(v[i].x * rinv * g0, v[i].y * rinv * g1);
-    o.y = pack_bf16x2(v[i].z * rinv * g2, v[i].w * rinv * g3);
+    o.x = pack_f16x2(v[i].x * rinv * g0, v[i].y * rinv * g1);
+    o.y = pack_f16x2(v[i].z * rinv * g2, v[i].w * rinv * g3);
     *reinterpret_cast<uint2*>(out + static_cast<size_t>(row) * kHidden + c) = o;
   }
 }
 
-// For a residual stream given directly: xa = bf16(x * (1 + s1[row])), plus the
+// For a residual stream given directly: xa = fp16(x * (1 + s1[row])), plus the
 // per-256-column sums of squares. One block per row; 16 consecutive columns per thread.
 __global__ void __launch_bounds__(256) block_prep_kernel(const float* __restrict__ x, int n_text,
                                                          const float* __restrict__ mod,
-                                                         __nv_bfloat16* __restrict__ xa, float* __restrict__ ssp) {
+                                                         act_t* __restrict__ xa, float* __restrict__ ssp) {
   const int row = blockIdx.x;
   const float* mrow = mod + (row < n_text ? kMod : 0);  // s1 is chunk 0
   const int c0 = threadIdx.x * 16;
@@ -134,8 +134,8 @@ __global__ void __launch_bounds__(256) block_prep_kernel(const float* __restrict
     const float4 v = xr[i];
     const float4 s = sr[i];
     ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-    packed[2 * i] = pack_bf16x2(v.x * (1.f + s.x), v.y * (1.f + s.y));
-    packed[2 * i + 1] = pack_bf16x2(v.z * (1.f + s.z), v.w * (1.f + s.w));
+    packed[2 * i] = pack_f16x2(v.x * (1.f + s.x), v.y * (1.f + s.y));
+    packed[2 * i + 1] = pack_f16x2(v.z * (1.f + s.z), v.w * (1.f + s.w));
   }
   uint4* dst = reinterpret_cast<uint4*>(xa + static_cast<size_t>(row) * kHidden + c0);
   dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
@@ -149,13 +149,13 @@ __global__ void __launch_bounds__(256) block_prep_kernel(const float* __restrict
 // ---------------------------------------------------------------- image projection
 
 // x[r] = img[r] . W^T + b (64 -> 4096) for image rows (sampled-t modulation),
-// xa = bf16(x * (1 + s1)), ssp = per-256-column sums of squares.
+// xa = fp16(x * (1 + s1)), ssp = per-256-column sums of squares.
 // Block: 256 columns (one per thread, its 64 weights in registers) x 64 rows.
 constexpr int kImgRows = 64;
 __global__ void __launch_bounds__(256) img_in_kernel(const float* __restrict__ img, int N,
                                                      const uint16_t* __restrict__ W, const uint16_t* __restrict__ b,
                                                      const float* __restrict__ mod, float* __restrict__ x,
-                                                     __nv_bfloat16* __restrict__ xa, float* __restrict__ ssp) {
+                                                     act_t* __restrict__ xa, float* __restrict__ ssp) {
   __shared__ float rows[kImgRows][kPatch];
   __shared__ float red[kImgRows][8];
   const int col = blockIdx.x * 256 + threadIdx.x;
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(256) img_in_kernel(const float* __restrict__ i
     acc += bias;
     const size_t idx = static_cast<size_t>(r0 + r) * kHidden + col;
     x[idx] = acc;
-    xa[idx] = __float2bfloat16_rn(acc * sc);
+    xa[idx] = __float2half_rn(acc * sc);
     const float s = warp_sum(acc * acc);
     if (lane == 0) red[r][warp] = s;
   }
@@ -210,7 +210,7 @@ constexpr int kHeadRows = 16;
 constexpr int kHeadK = 128;
 __global__ void __launch_bounds__(256) head_kernel(const float* __restrict__ x, int N, const float* __restrict__ ssp,
                                                    const uint16_t* __restrict__ W, const uint16_t* __restrict__ b,
-                                                   float* __restrict__ vel) {
+                                                   float* __restrict__ vel, int* err) {
   __shared__ float wt[kHeadK][kPatch + 1];
   __shared__ float xs[kHeadRows][kHeadK + 1];
   const int r0 = blockIdx.x * kHeadRows;
@@ -252,7 +252,10 @@ __global__ void __launch_bounds__(256) head_kernel(const float* __restrict__ x, 
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int o = oq + 16 * j;
-      vel[static_cast<size_t>(row) * kPatch + o] = acc[j] * rinv + bf16_bits_to_float(b[o]);
+      const float v = acc[j] * rinv + bf16_bits_to_float(b[o]);
+      vel[static_cast<size_t>(row) * kPatch + o] = v;
+      // guard: a non-finite velocity (e.g. an fp16 operand that left its range) is reported
+      if (!isfinite(v)) report_error(err, kErrNonFinite);
     }
   }
 }
@@ -354,6 +357,22 @@ __global__ void pack_noise_kernel(const float* __restrict__ z, int T, float* __r
   }
 }
 
+// In place bf16 -> fp16 conversion of a weight tensor, two values per thread
+// step. fp16 holds every bf16 value of magnitude 2^-14..65504 exactly; smaller
+// ones round to fp16 subnormals (error < 2^-25); larger ones are counted.
+__global__ void bf16_to_f16_kernel(uint32_t* w, size_t pairs, unsigned int* overflow) {
+  unsigned int bad = 0;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < pairs;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint32_t v = w[i];
+    const float lo = __uint_as_float(v << 16);
+    const float hi = __uint_as_float(v & 0xFFFF0000u);
+    bad += (fabsf(lo) > 65504.f) + (fabsf(hi) > 65504.f);
+    w[i] = pack_f16x2(lo, hi);
+  }
+  if (bad) atomicAdd(overflow, bad);
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- launchers
@@ -376,13 +395,13 @@ cudaError_t launch_gemv2(const float* x, int in_dim, const uint16_t* W, const ui
   return cudaGetLastError();
 }
 
-cudaError_t launch_txt_prenorm(const float* txt, int L, const uint16_t* w, __nv_bfloat16* out, cudaStream_t s) {
+cudaError_t launch_txt_prenorm(const float* txt, int L, const uint16_t* w, act_t* out, cudaStream_t s) {
   if (L <= 0) return cudaSuccess;
   txt_prenorm_kernel<<<L, 256, 0, s>>>(txt, w, out);
   return cudaGetLastError();
 }
 
-cudaError_t launch_block_prep(const float* x, int R, int n_text, const float* mod, __nv_bfloat16* xa, float* ssp,
+cudaError_t launch_block_prep(const float* x, int R, int n_text, const float* mod, act_t* xa, float* ssp,
                               cudaStream_t s) {
   if (R <= 0) return cudaSuccess;
   block_prep_kernel<<<R, 256, 0, s>>>(x, n_text, mod, xa, ssp);
@@ -390,7 +409,7 @@ cudaError_t launch_block_prep(const float* x, int R, int n_text, const float* mo
 }
 
 cudaError_t launch_img_in(const float* img, int N, const uint16_t* W, const uint16_t* b, const float* mod, float* x,
-                          __nv_bfloat16* xa, float* ssp, cudaStream_t s) {
+                          act_t* xa, float* ssp, cudaStream_t s) {
   if (N <= 0) return cudaSuccess;
   dim3 grid(kHidden / 256, (N + kImgRows - 1) / kImgRows);
   img_in_kernel<<<grid, 256, 0, s>>>(img, N, W, b, mod, x, xa, ssp);
@@ -398,9 +417,18 @@ cudaError_t launch_img_in(const float* img, int N, const uint16_t* W, const uint
 }
 
 cudaError_t launch_head(const float* x, int N, const float* ssp, const uint16_t* W, const uint16_t* b, float* vel,
-                        cudaStream_t s) {
+                        int* err, cudaStream_t s) {
   if (N <= 0) return cudaSuccess;
-  head_kernel<<<(N + kHeadRows - 1) / kHeadRows, 256, 0, s>>>(x, N, ssp, W, b, vel);
+  head_kernel<<<(N + kHeadRows - 1) / kHeadRows, 256, 0, s>>>(x, N, ssp, W, b, vel, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bf16_to_f16(uint16_t* w, size_t n, unsigned int* overflow, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const size_t pairs = n / 2;  // weight tensors here have an even element count
+  const size_t want = (pairs + 255) / 256;
+  const unsigned blocks = static_cast<unsigned>(want < 148 * 32 ? want : 148 * 32);
+  bf16_to_f16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<uint32_t*>(w), pairs, overflow);
   return cudaGetLastError();
 }
 

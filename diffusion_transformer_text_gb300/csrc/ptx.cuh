@@ -3,6 +3,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 namespace qi {
@@ -11,13 +12,7 @@ namespace qi {
 // an error in the device error word and its kernel winds down.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
-enum DeviceError : int {
-  kErrNone = 0,
-  kErrTimeoutProducer = 1,
-  kErrTimeoutMma = 2,
-  kErrTimeoutEpilogue = 3,
-  kErrTimeoutDrain = 4,
-};
+// (device error codes: DeviceError in internal.h)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -134,7 +129,7 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor for a K-major bf16 tile written by TMA with
+// Shared-memory matrix descriptor for a K-major 16-bit tile written by TMA with
 // 128-byte swizzle: rows of 64 elements (128 B), 8-row groups 1024 B apart.
 // Bits: [0,14) start >> 4, [16,30) leading byte offset >> 4 (unused for this
 // layout, set to 1), [32,46) stride byte offset >> 4, bit 46 descriptor
@@ -156,8 +151,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Same with fp16 A and B (format code 0 in bits 7-9 and 10-12).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -228,9 +228,9 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// D[tmem] (+)= A[tmem] * B[smem]: the A operand (M lanes x K, two bf16 per
+// D[tmem] (+)= A[tmem] * B[smem]: the A operand (M lanes x K, two 16-bit values per
 // 32-bit column) is read from tensor memory. Issued by one thread.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -240,7 +240,7 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
-// Shared-memory descriptor for an MN-major bf16 operand written by TMA with
+// Shared-memory descriptor for an MN-major 16-bit operand written by TMA with
 // 128-byte swizzle: each 128-byte line holds 64 consecutive MN elements of one
 // K row; 8-row groups along K are `sbo` bytes apart and 64-element chunks along
 // MN are `lbo` bytes apart.
@@ -259,6 +259,8 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) {
   return idesc_bf16_f32(M, N) | (1u << 16);
 }
 
+__host__ __device__ constexpr uint32_t idesc_f16_f32_bmn(int M, int N) { return idesc_f16_f32(M, N) | (1u << 16); }
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -269,6 +271,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 

@@ -7,7 +7,9 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
+#include <utility>
 #include <string>
 #include <vector>
 
@@ -22,7 +24,7 @@ using qi::kPatch;
 using qi::kRopeCols;
 using qi::kSspParts;
 using qi::kTdim;
-using bf16 = __nv_bfloat16;
+using qi::act_t;
 
 namespace {
 
@@ -72,13 +74,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 map over a row-major [rows, cols] matrix; box = box_rows x 64 columns
-// (one 128-byte swizzle span), rows past `rows` read as zero.
-qi_status make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// 2-D 16-bit map over a row-major [rows, cols] matrix (fp16 unless `bf16`); box =
+// box_rows x 64 columns (one 128-byte swizzle span), rows past `rows` read as zero.
+qi_status make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                   bool bf16 = false) {
   if (!encode_fn()) return fail(QI_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (cols * 2) % 16 != 0)
     return fail(QI_ERR_INVALID_ARG, "tensor map base or row pitch not 16-byte aligned");
-  if (!qi::encode_bf16_map(m, base, rows, cols, box_rows)) return fail(QI_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  if (!qi::encode_map16(m, base, rows, cols, box_rows, bf16)) return fail(QI_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   return QI_OK;
 }
 
@@ -112,18 +115,19 @@ struct qi_dit {
   // activations (one allocation)
   void* amem = nullptr;
   float* x = nullptr;      // [R_max, 4096] fp32 residual stream
-  bf16* xa = nullptr;      // [R_max, 4096] bf16 modulated GEMM input
+  act_t* xa = nullptr;     // [R_max, 4096] fp16 modulated GEMM input
   float* ssp = nullptr;    // [R_max, 16] sum-of-squares partials
-  bf16* q = nullptr;       // [R_max, 4096]
-  bf16* o = nullptr;       // [R_max, 4096] attention output
-  bf16* h = nullptr;       // [R_max, 12288] SwiGLU hidden
-  bf16* txt_a = nullptr;   // [L_max, 4096] text pre-norm output
+  act_t* q = nullptr;      // [R_max, 4096]
+  act_t* o = nullptr;      // [R_max, 4096] attention output
+  act_t* h = nullptr;      // [R_max, 12288] SwiGLU hidden
+  act_t* txt_a = nullptr;  // [L_max, 4096] text pre-norm output
   float* temb_e = nullptr; // [2, 256]
   float* temb_h = nullptr; // [2, 4096]
   float* temb = nullptr;   // [2, 4096]
   float* mod = nullptr;    // [2, 16384]: row 0 sampled t, row 1 t = 0
   int* err = nullptr;      // device error word
-  bf16* kv = nullptr;      // [blocks][2][R_max][4096]
+  act_t* kv = nullptr;     // [blocks][2][R_max][4096] fp16
+  unsigned int* ovf = nullptr;  // weight values outside the fp16 range seen at load
   int cache_L = -1;        // L of the valid text K/V capture, -1 if none
 
   // host-I/O staging (allocated on first use)
@@ -141,8 +145,8 @@ struct qi_dit {
   std::vector<ProfEv> prof_ev;
   size_t prof_used = 0;
 
-  bf16* k_of(int b) { return kv + static_cast<size_t>(b) * 2 * R_max * kHidden; }
-  bf16* v_of(int b) { return k_of(b) + static_cast<size_t>(R_max) * kHidden; }
+  act_t* k_of(int b) { return kv + static_cast<size_t>(b) * 2 * R_max * kHidden; }
+  act_t* v_of(int b) { return k_of(b) + static_cast<size_t>(R_max) * kHidden; }
 };
 
 namespace {
@@ -178,6 +182,7 @@ qi_status check_device_word(qi_dit* d, cudaStream_t s) {
   if (h != 0) {
     QI_CUDA(cudaMemsetAsync(d->err, 0, sizeof(int), s));
     QI_CUDA(cudaStreamSynchronize(s));
+    if (h == qi::kErrNonFinite) return fail(QI_ERR_NONFINITE, "the DiT pass produced a non-finite velocity");
     return fail(QI_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired (device code %d)", h);
   }
   return QI_OK;
@@ -240,7 +245,7 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
     a.err = d->err;
     QI_CUDA(qi::launch_attention(a, s));
   }
-  // out-projection: x += g1 * (o Wo^T); xa = bf16(x (1 + s2))
+  // out-projection: x += g1 * (o Wo^T); xa = fp16(x (1 + s2))
   {
     ProfScope ps(d, s, 2);
     qi::GemmParams g = p;
@@ -264,7 +269,7 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
     g.h = d->h;
     QI_CUDA(qi::launch_gemm(qi::kEpiSwiglu, m_xa, B.m_gu, g, d->num_sms, s));
   }
-  // down: x += g2 * (h Wd^T); xa = bf16(x (1 + s1)) for the next block
+  // down: x += g2 * (h Wd^T); xa = fp16(x (1 + s1)) for the next block
   {
     ProfScope ps(d, s, 4);
     qi::GemmParams g = p;
@@ -340,8 +345,21 @@ qi_status run_pass(qi_dit* d, PassMode mode, const float* img, int N, const floa
   if (n_img > 0) {
     ProfScope ps(d, s, 5);
     const size_t off = static_cast<size_t>(n_text);
-    QI_CUDA(qi::launch_head(d->x + off * kHidden, N, d->ssp + off * kSspParts, d->out_w, d->out_b, vel, s));
+    QI_CUDA(qi::launch_head(d->x + off * kHidden, N, d->ssp + off * kSspParts, d->out_w, d->out_b, vel, d->err, s));
   }
+  return QI_OK;
+}
+
+// bf16 -> fp16 in place for tensor-core weights; synchronises `s`. A value beyond
+// the fp16 range (|w| > 65504) makes the load fail.
+qi_status convert_weights(qi_dit* d, std::initializer_list<std::pair<uint16_t*, size_t>> tensors, cudaStream_t s,
+                          const char* who) {
+  QI_CUDA(cudaMemsetAsync(d->ovf, 0, sizeof(unsigned int), s));
+  for (auto& t : tensors) QI_CUDA(qi::launch_bf16_to_f16(t.first, t.second, d->ovf, s));
+  unsigned int bad = 0;
+  QI_CUDA(cudaMemcpyAsync(&bad, d->ovf, sizeof(bad), cudaMemcpyDeviceToHost, s));
+  QI_CUDA(cudaStreamSynchronize(s));
+  if (bad) return fail(QI_ERR_INVALID_ARG, "%s: %u weight values exceed the fp16 range (|w| > 65504)", who, bad);
   return QI_OK;
 }
 
@@ -356,14 +374,15 @@ bool all_loaded(const qi_dit* d) {
 
 void qi::set_last_error(const char* msg) { g_last_error = msg; }
 
-bool qi::encode_bf16_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+bool qi::encode_map16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows, bool bf16) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || (reinterpret_cast<uintptr_t>(base) & 15) != 0 || (cols * 2) % 16 != 0 || rows == 0) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -445,7 +464,7 @@ qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out) {
       {(void**)&d->o, R * kHidden * 2},   {(void**)&d->h, R * kFfn * 2},
       {(void**)&d->txt_a, (size_t)d->L_max * kHidden * 2}, {(void**)&d->temb_e, 2 * kTdim * 4},
       {(void**)&d->temb_h, 2 * kHidden * 4}, {(void**)&d->temb, 2 * kHidden * 4},
-      {(void**)&d->mod, 2 * (size_t)kMod * 4}, {(void**)&d->err, 256},
+      {(void**)&d->mod, 2 * (size_t)kMod * 4}, {(void**)&d->err, 256}, {(void**)&d->ovf, 256},
       {(void**)&d->kv, (size_t)cfg->blocks * 2 * R * kHidden * 2},
   };
   size_t abytes = 0;
@@ -523,7 +542,8 @@ qi_status qi_dit_load_global(qi_dit* d, const qi_global_weights* w, int src_on_d
   QI_CUDA(cudaSetDevice(d->device));
   const cudaMemcpyKind kind = src_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
   for (int i = 0; i < 13; ++i) QI_CUDA(cudaMemcpyAsync(dst[i], src[i], n[i] * 2, kind, s));
-  QI_CUDA(cudaStreamSynchronize(s));
+  // the text projection runs on the tensor cores with fp16 operands
+  QI_TRY(convert_weights(d, {{d->txt_w, (size_t)kHidden * kHidden}}, s, "qi_dit_load_global"));
   d->loaded_global = true;
   return QI_OK;
 }
@@ -549,7 +569,9 @@ qi_status qi_dit_load_block(qi_dit* d, int block, const qi_block_weights* w, int
   QI_CUDA(cudaMemcpy2DAsync(reinterpret_cast<char*>(B.wgu) + grp, 2 * grp, w->wu, grp, grp, kFfn / (kBN / 2), kind,
                             s));
   QI_CUDA(cudaMemcpyAsync(B.wd, w->wd, (size_t)kHidden * kFfn * 2, kind, s));
-  QI_CUDA(cudaStreamSynchronize(s));
+  QI_TRY(convert_weights(d,
+                         {{B.wqkv, 3 * sq}, {B.wo, sq}, {B.wgu, (size_t)2 * kFfn * kHidden}, {B.wd, (size_t)kHidden * kFfn}},
+                         s, "qi_dit_load_block"));
   d->loaded_block[block] = true;
   return QI_OK;
 }
@@ -730,8 +752,8 @@ qi_status qi_gemm_bf16(qi_dit* d, const uint16_t* A, const uint16_t* B, float* D
   if (M < 1 || N < kBN || N % kBN != 0 || K < qi::kBK || K % qi::kBK != 0)
     return fail(QI_ERR_SHAPE, "qi_gemm_bf16: M %d N %d K %d", M, N, K);
   CUtensorMap ma, mb;
-  QI_TRY(make_map(&ma, A, M, K, 128));
-  QI_TRY(make_map(&mb, B, N, K, 256));
+  QI_TRY(make_map(&ma, A, M, K, 128, true));
+  QI_TRY(make_map(&mb, B, N, K, 256, true));
   qi::GemmParams g{};
   g.M = M;
   g.N = N;
@@ -743,16 +765,16 @@ qi_status qi_gemm_bf16(qi_dit* d, const uint16_t* A, const uint16_t* B, float* D
   return QI_OK;
 }
 
-qi_status qi_attention_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, int Rq, int q_off,
+qi_status qi_attention_f16(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, int Rq, int q_off,
                             int L, int Lk, qi_stream_t stream) {
-  if (!q || !k || !v || !o) return fail(QI_ERR_INVALID_ARG, "qi_attention_bf16: NULL argument");
+  if (!q || !k || !v || !o) return fail(QI_ERR_INVALID_ARG, "qi_attention_f16: NULL argument");
   if (Rq < 0 || q_off < 0 || L < 0 || Lk < 1 || L > Lk || q_off + Rq > Lk)
-    return fail(QI_ERR_SHAPE, "qi_attention_bf16: Rq %d q_off %d L %d Lk %d", Rq, q_off, L, Lk);
+    return fail(QI_ERR_SHAPE, "qi_attention_f16: Rq %d q_off %d L %d Lk %d", Rq, q_off, L, Lk);
   qi::AttnParams a{};
-  a.q = reinterpret_cast<const bf16*>(q);
-  a.k = reinterpret_cast<const bf16*>(k);
-  a.v = reinterpret_cast<const bf16*>(v);
-  a.o = reinterpret_cast<bf16*>(o);
+  a.q = reinterpret_cast<const act_t*>(q);
+  a.k = reinterpret_cast<const act_t*>(k);
+  a.v = reinterpret_cast<const act_t*>(v);
+  a.o = reinterpret_cast<act_t*>(o);
   a.Rq = Rq;
   a.q_off = q_off;
   a.L = L;

@@ -22,7 +22,11 @@
  *   - Tensor arguments are DEVICE pointers (memory of the device the handle was
  *     created on) unless the argument says "host".
  *   - Floating-point tensors crossing the boundary are float32, row-major.
- *     Weights are bfloat16 bit patterns (uint16_t), row-major [out, in].
+ *     Weights are bfloat16 bit patterns (uint16_t), row-major [out, in]. The
+ *     library keeps the tensor-core weights as fp16 (converted once at load:
+ *     exact for |w| >= 2^-14, error < 2^-25 below; |w| > 65504 is rejected) and
+ *     runs every tensor-core product on fp16 operands with fp32 accumulation;
+ *     the residual stream, norms and modulation stay fp32.
  *   - Work is enqueued on `stream` (0 = legacy default stream); calls return
  *     without synchronising unless stated. The caller owns every buffer it
  *     passes; the library never keeps a caller pointer after a call returns.
@@ -52,7 +56,8 @@ typedef enum qi_status {
   QI_ERR_OOM = 4,             /* device allocation failed                       */
   QI_ERR_CUDA = 5,            /* a CUDA runtime/driver call failed              */
   QI_ERR_DEVICE_TIMEOUT = 6,  /* a kernel's bounded wait expired (device word)  */
-  QI_ERR_NOT_IMPLEMENTED = 7
+  QI_ERR_NOT_IMPLEMENTED = 7,
+  QI_ERR_NONFINITE = 8        /* a pass produced a non-finite velocity (device word) */
 } qi_status;
 
 /* Model widths [ARCH]. head_dim 128 follows from the 64 RoPE columns per token
@@ -221,8 +226,9 @@ qi_status qi_text_kv_capture(qi_dit* dit, const float* txt_feats, int L, const f
  * 2 x blocks x L x 4096 x 2. */
 size_t qi_kv_cache_bytes(int blocks, int L);
 
-/* Device error word: synchronises `stream`, returns DEVICE_TIMEOUT (and clears
- * the word) if a kernel's bounded wait expired since the last check. */
+/* Device error word: synchronises `stream`; returns DEVICE_TIMEOUT if a kernel's
+ * bounded wait expired, or NONFINITE if a pass produced a non-finite velocity,
+ * since the last check (and clears the word). */
 qi_status qi_dit_check(qi_dit* dit, qi_stream_t stream);
 
 /* ------------------------------------------------------------------ test hooks */
@@ -233,7 +239,7 @@ qi_status qi_dit_check(qi_dit* dit, qi_stream_t stream);
 qi_status qi_dit_block_forward(qi_dit* dit, int block, float* hidden, int L, int N, float t_img,
                                const float* cos, const float* sin, qi_stream_t stream);
 
-/* Copy rows [row0, row0 + rows) of block `block`'s stored K and V (bf16 bits,
+/* Copy rows [row0, row0 + rows) of block `block`'s stored K and V (fp16 bits,
  * [rows, 4096] each, device) into k_out / v_out. After a pass, rows [0, L) are
  * the text K/V (post-RoPE K) and rows [L, L + N) the image K/V of that pass.
  * Errors: INVALID_ARG (block, NULL), SHAPE (rows past L_max + N_max). */
@@ -268,10 +274,10 @@ qi_status qi_gemm_bf16_noalloc(const uint16_t* A, const uint16_t* B, float* D, i
                                int sync_check, qi_stream_t stream);
 
 /* The block-causal attention kernel on its own (test hook). q [Rq, 4096],
- * k/v [Lk, 4096], o [Rq, 4096], bf16 bits, 32 heads x 128 (device). Query row
+ * k/v [Lk, 4096], o [Rq, 4096], fp16 bits, 32 heads x 128 (device). Query row
  * r has global index r + q_off: if that is < L it sees keys 0..index (text,
  * causal), otherwise keys 0..Lk-1. Scale 1/sqrt(128). */
-qi_status qi_attention_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, int Rq,
+qi_status qi_attention_f16(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, int Rq,
                             int q_off, int L, int Lk, qi_stream_t stream);
 
 /* During later qi_dit_step calls, copy the float32 residual stream entering

@@ -45,3 +45,14 @@ def bf16_tensor(bits, device="cuda"):
 def f32_tensor(a, device="cuda"):
     import torch
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
+
+
+def f16_tensor(a, device="cuda"):
+    """float32 values -> fp16 device tensor (int16 view of the fp16 bits)."""
+    import torch
+    h = np.ascontiguousarray(np.asarray(a, np.float32).astype(np.float16))
+    return torch.from_numpy(h.view(np.int16)).to(device)
+
+
+def f16_bits_to_f32(bits):
+    return np.ascontiguousarray(bits).view(np.float16).astype(np.float32)

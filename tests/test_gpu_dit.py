@@ -6,7 +6,7 @@ import synth
 from oracle import dit as odit
 from oracle import rope as orope
 
-from gpu_util import assert_close, f32_tensor, load_weights
+from gpu_util import assert_close, f16_bits_to_f32, f32_tensor, load_weights
 
 pytestmark = pytest.mark.gpu
 
@@ -48,8 +48,8 @@ def test_one_block(qi):
         # the residual carries the input through; judge the block's update
         assert_close(got - x, ref - x, "block update")
         k, v = d.read_kv(0, 0, case.L + case.N)
-        k = synth.bf16_bits_to_f32(k.cpu().numpy().view(np.uint16))
-        v = synth.bf16_bits_to_f32(v.cpu().numpy().view(np.uint16))
+        k = f16_bits_to_f32(k.cpu().numpy())
+        v = f16_bits_to_f32(v.cpu().numpy())
         assert_close(k, rk.reshape(case.L + case.N, -1), "stored K (post-RoPE)")
         assert_close(v, rv.reshape(case.L + case.N, -1), "stored V")
     finally:
@@ -111,6 +111,51 @@ def test_text_only_capture_equals_joint(qi, dit256):
     for (jk, jv), b in zip(joint, (0, 13, 31)):
         k, v = d.read_kv(b, 0, case.L)
         assert np.array_equal(jk, k.cpu().numpy()) and np.array_equal(jv, v.cpu().numpy())
+
+
+def test_weight_outside_fp16_range_is_rejected(qi):
+    """Tensor-core weights are kept as fp16: a bf16 value beyond +-65504 fails the load."""
+    d = qi.DiT(blocks=1, L_max=8, N_max=64)
+    try:
+        W = synth.Weights(seed=0, nblocks=1)
+        g = dict(W.glob)
+        txt_w = g["txt_w"].copy()
+        txt_w[5, 7] = synth.f32_to_bf16_bits(np.array([1.0e5], np.float32))[0]
+        g["txt_w"] = txt_w
+        with pytest.raises(qi.QiError) as e:
+            d.load_global(g)
+        assert e.value.status == 1 and "fp16 range" in str(e.value)
+        bw = dict(W.block(0))
+        wd = bw["wd"].copy()
+        wd[0, 0] = synth.f32_to_bf16_bits(np.array([-7.0e4], np.float32))[0]
+        bw["wd"] = wd
+        with pytest.raises(qi.QiError) as e:
+            d.load_block(0, bw)
+        assert e.value.status == 1
+    finally:
+        d.close()
+
+
+def test_nonfinite_velocity_is_reported(qi):
+    """A NaN planted in a bias reaches the velocity; the head's guard reports it."""
+    case = synth.BLOCK_CASE
+    d = qi.DiT(blocks=1, L_max=case.L, N_max=case.N)
+    try:
+        W = synth.Weights(seed=0, nblocks=1)
+        g = dict(W.glob)
+        img_b = g["img_b"].copy()
+        img_b[3] = 0x7FC0  # bf16 quiet NaN
+        g["img_b"] = img_b
+        d.load_global(g)
+        d.load_block(0, W.block(0))
+        tc, ts, ic, is_ = [f32_tensor(a) for a in _tables(case.L, case.h, case.w)]
+        d.step(f32_tensor(synth.img_tokens(case)), f32_tensor(synth.txt_feats(case)), 0.5, tc, ts, ic, is_)
+        with pytest.raises(qi.QiError) as e:
+            d.check()
+        assert e.value.status == 8
+        d.check()  # the word was cleared by the report
+    finally:
+        d.close()
 
 
 def test_use_cache_requires_capture(qi):

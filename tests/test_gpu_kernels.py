@@ -7,7 +7,7 @@ from oracle import attention as oatt
 from oracle import rope as orope
 from oracle import sched as osched
 
-from gpu_util import assert_close, bf16_tensor, f32_tensor
+from gpu_util import assert_close, bf16_tensor, f16_bits_to_f32, f16_tensor, f32_tensor
 
 pytestmark = pytest.mark.gpu
 
@@ -60,23 +60,23 @@ def test_gemm_rows_independent_of_m(qi, small_dit):
 # ---------------------------------------------------------------- attention
 
 def _qkv(R, seed):
-    q = synth.weight_bf16(seed, 0, (R, 4096), std=1.3)
-    k = synth.weight_bf16(seed, 1, (R, 4096), std=1.3)
-    v = synth.weight_bf16(seed, 2, (R, 4096), std=1.0)
-    return q, k, v
+    """fp16-valued q, k, v [R, 4096] (float32 arrays holding fp16 values)."""
+    q = synth.normal_f32(seed, 0, R * 4096, np.float32(1.3)).astype(np.float16).astype(np.float32)
+    k = synth.normal_f32(seed, 1, R * 4096, np.float32(1.3)).astype(np.float16).astype(np.float32)
+    v = synth.normal_f32(seed, 2, R * 4096).astype(np.float16).astype(np.float32)
+    return q.reshape(R, 4096), k.reshape(R, 4096), v.reshape(R, 4096)
 
 
 def _oracle_att(q, k, v, L):
     R = q.shape[0]
-    f = lambda a: synth.bf16_bits_to_f32(a).reshape(R, 32, 128)
-    return oatt.attention_masked(f(q), f(k), f(v), L)
+    return oatt.attention_masked(q.reshape(R, 32, 128), k.reshape(R, 32, 128), v.reshape(R, 32, 128), L)
 
 
 @pytest.mark.parametrize("L,N", [(7, 150), (1, 64), (130, 70), (22, 256)])
 def test_attention_joint(qi, L, N):
     q, k, v = _qkv(L + N, L + N)
-    o = qi.attention(bf16_tensor(q), bf16_tensor(k), bf16_tensor(v), L)
-    got = synth.bf16_bits_to_f32(o.cpu().numpy().view(np.uint16))
+    o = qi.attention(f16_tensor(q), f16_tensor(k), f16_tensor(v), L)
+    got = f16_bits_to_f32(o.cpu().numpy())
     ref = _oracle_att(q, k, v, L)
     assert_close(got.reshape(L + N, -1), ref, f"attention L={L} N={N}")
 
@@ -85,7 +85,7 @@ def test_attention_image_only_equals_joint(qi):
     """Image rows against stored text K/V give the joint pass's image rows bit for bit."""
     L, N = 37, 200
     q, k, v = _qkv(L + N, 5)
-    qt, kt, vt = bf16_tensor(q), bf16_tensor(k), bf16_tensor(v)
+    qt, kt, vt = f16_tensor(q), f16_tensor(k), f16_tensor(v)
     joint = qi.attention(qt, kt, vt, L).cpu().numpy()
     img = qi.attention(qt[L:].contiguous(), kt, vt, L, q_off=L).cpu().numpy()
     assert np.array_equal(joint[L:], img)
@@ -98,8 +98,8 @@ def test_attention_long_keys(qi):
     """Several query and key tiles with a ragged tail at a realistic head count."""
     L, N = 407, 600
     q, k, v = _qkv(L + N, 9)
-    o = qi.attention(bf16_tensor(q), bf16_tensor(k), bf16_tensor(v), L)
-    got = synth.bf16_bits_to_f32(o.cpu().numpy().view(np.uint16))
+    o = qi.attention(f16_tensor(q), f16_tensor(k), f16_tensor(v), L)
+    got = f16_bits_to_f32(o.cpu().numpy())
     assert_close(got, _oracle_att(q, k, v, L), "attention 407+600")
 
 
