@@ -39,6 +39,7 @@ SYMBOLS = (
     "qi_dit_step", "qi_text_kv_capture", "qi_kv_cache_bytes", "qi_dit_check",
     "qi_dit_block_forward", "qi_dit_read_kv", "qi_dit_set_trace", "qi_dit_profile",
     "qi_dit_profile_read", "qi_last_error", "qi_gemm_bf16", "qi_attention_f16", "qi_gemm_bf16_noalloc",
+    "qi_dit_step_cfg",
 )
 
 
@@ -49,7 +50,7 @@ class QiError(RuntimeError):
 
 
 class DitConfig(ctypes.Structure):
-    _fields_ = [("blocks", ctypes.c_int), ("L_max", ctypes.c_int), ("N_max", ctypes.c_int)]
+    _fields_ = [("blocks", ctypes.c_int), ("L_max", ctypes.c_int), ("N_max", ctypes.c_int), ("kv_slots", ctypes.c_int)]
 
 
 _GLOBAL_FIELDS = ("t_w1", "t_b1", "t_w2", "t_b2", "mod_w", "mod_b", "txt_norm_w", "txt_w", "txt_b",
@@ -104,6 +105,7 @@ def lib() -> ctypes.CDLL:
         "qi_gemm_bf16": [P, P, P, P, I, I, I, P],
         "qi_attention_f16": [P, P, P, P, I, I, I, I, P],
         "qi_gemm_bf16_noalloc": [P, P, P, I, I, I, I, P],
+        "qi_dit_step_cfg": [P, P, I, F, F, P, I, P, P, P, P, P, I, P, P, P, P, P, U, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -216,10 +218,10 @@ def attention(q, k, v, L: int, q_off: int = 0, Lk: int | None = None):
 class DiT:
     """A qi_dit handle: bf16 weight store, activations and per-block text K/V."""
 
-    def __init__(self, blocks: int = 32, L_max: int = 512, N_max: int = 4096, device: int = 0):
+    def __init__(self, blocks: int = 32, L_max: int = 512, N_max: int = 4096, device: int = 0, kv_slots: int = 1):
         self.blocks, self.L_max, self.N_max, self.device = blocks, L_max, N_max, device
         h = ctypes.c_void_p()
-        _check(lib().qi_dit_create(ctypes.byref(DitConfig(blocks, L_max, N_max)), device, ctypes.byref(h)))
+        _check(lib().qi_dit_create(ctypes.byref(DitConfig(blocks, L_max, N_max, kv_slots)), device, ctypes.byref(h)))
         self._h = h
 
     def close(self):
@@ -306,6 +308,24 @@ class DiT:
         flags = STEP_HOST_IO | (STEP_USE_CACHE if use_cache else 0)
         _check(lib().qi_dit_step(self._h, hp(img_tokens), N, hp(txt_feats), L, float(timestep), hp(txt_cos),
                                  hp(txt_sin), hp(img_cos), hp(img_sin), hp(vel), flags, _stream(stream)))
+        return vel
+
+    def step_cfg(self, img_tokens, timestep: float, guidance: float, pos, neg, use_cache: bool = False, vel=None,
+                 stream=None):
+        """Classifier-free guidance step. pos / neg: dicts with keys feats (or None
+        with use_cache), L, txt_cos, txt_sin, img_cos, img_sin (device tensors)."""
+        import torch
+        N = img_tokens.shape[0]
+        _dev_f32(img_tokens, (N, PATCH), "img_tokens")
+        if vel is None:
+            vel = torch.empty(N, PATCH, device=img_tokens.device, dtype=torch.float32)
+        g = lambda d, k: None if use_cache and k in ("feats", "txt_cos", "txt_sin") else _ptr(d.get(k))
+        _check(lib().qi_dit_step_cfg(
+            self._h, _ptr(img_tokens), N, float(timestep), float(guidance),
+            g(pos, "feats"), int(pos["L"]), g(pos, "txt_cos"), g(pos, "txt_sin"), _ptr(pos["img_cos"]),
+            _ptr(pos["img_sin"]), g(neg, "feats"), int(neg["L"]), g(neg, "txt_cos"), g(neg, "txt_sin"),
+            _ptr(neg["img_cos"]), _ptr(neg["img_sin"]), _ptr(vel), STEP_USE_CACHE if use_cache else STEP_JOINT,
+            _stream(stream)))
         return vel
 
     def text_kv_capture(self, txt_feats, txt_cos, txt_sin, stream=None):

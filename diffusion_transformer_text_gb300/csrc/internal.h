@@ -119,6 +119,9 @@ cudaError_t launch_rope_axis(float theta, float* c0, float* s0, float* c1, float
 cudaError_t launch_rope_tokens(int L, int h, int w, float theta, float* tc, float* ts, float* ic, float* is,
                                cudaStream_t s);
 cudaError_t launch_pack_noise(const float* z, int h, int w, float* x, cudaStream_t s);
+// Classifier-free guidance: out = neg + g * (pos - neg), each operation rounded
+// on its own (no FMA contraction).
+cudaError_t launch_cfg_combine(const float* pos, const float* neg, float g, float* out, long long n, cudaStream_t s);
 // In place bf16 -> fp16 for a weight tensor of n elements; values whose
 // magnitude exceeds the fp16 range are counted into *overflow.
 cudaError_t launch_bf16_to_f16(uint16_t* w, size_t n, unsigned int* overflow, cudaStream_t s);

@@ -342,6 +342,12 @@ __global__ void euler_kernel(float* __restrict__ x, const float* __restrict__ ve
   }
 }
 
+__global__ void cfg_combine_kernel(const float* __restrict__ pos, const float* __restrict__ neg, float g,
+                                   float* __restrict__ out, long long n) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = __fadd_rn(neg[i], __fmul_rn(g, __fsub_rn(pos[i], neg[i])));
+}
+
 // x[t, c] = z[c, t] for t < h*w, c < 64 (32x32 tiles through shared memory).
 __global__ void pack_noise_kernel(const float* __restrict__ z, int T, float* __restrict__ x) {
   __shared__ float tile[32][33];
@@ -450,6 +456,12 @@ cudaError_t launch_rope_tokens(int L, int h, int w, float theta, float* tc, floa
   const int T = L + h * w;
   if (T <= 0) return cudaSuccess;
   rope_tokens_kernel<<<T, 64, 0, s>>>(L, h, w, static_cast<double>(theta), tc, ts, ic, is);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cfg_combine(const float* pos, const float* neg, float g, float* out, long long n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  cfg_combine_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(pos, neg, g, out, n);
   return cudaGetLastError();
 }
 

@@ -128,7 +128,11 @@ struct qi_dit {
   int* err = nullptr;      // device error word
   act_t* kv = nullptr;     // [blocks][2][R_max][4096] fp16
   unsigned int* ovf = nullptr;  // weight values outside the fp16 range seen at load
-  int cache_L = -1;        // L of the valid text K/V capture, -1 if none
+  int slots = 1;           // text K/V slots: 1, or 2 for classifier-free guidance
+  int cur_slot = 0;        // slot the running pass reads and writes
+  int cache_L[2] = {-1, -1};  // per slot: L of the valid text K/V capture, -1 if none
+  float* vel_pos = nullptr;   // [N_max, 64] guidance: conditional velocity (slots == 2)
+  float* vel_neg = nullptr;   // [N_max, 64] guidance: negative-prompt velocity
 
   // host-I/O staging (allocated on first use)
   float *st_img = nullptr, *st_txt = nullptr, *st_tc = nullptr, *st_ts = nullptr, *st_ic = nullptr,
@@ -145,7 +149,7 @@ struct qi_dit {
   std::vector<ProfEv> prof_ev;
   size_t prof_used = 0;
 
-  act_t* k_of(int b) { return kv + static_cast<size_t>(b) * 2 * R_max * kHidden; }
+  act_t* k_of(int b) { return kv + (static_cast<size_t>(cur_slot) * blocks + b) * 2 * R_max * kHidden; }
   act_t* v_of(int b) { return k_of(b) + static_cast<size_t>(R_max) * kHidden; }
 };
 
@@ -296,9 +300,10 @@ qi_status trace_copy(qi_dit* d, int at_block, int R, cudaStream_t s) {
 
 // The whole pass. Joint: rows [text L | image N]; image: rows [image N] with the
 // stored text K/V; text: rows [text L], no head.
-qi_status run_pass(qi_dit* d, PassMode mode, const float* img, int N, const float* txt, int L, float t,
+qi_status run_pass(qi_dit* d, int slot, PassMode mode, const float* img, int N, const float* txt, int L, float t,
                    const float* tc, const float* ts, const float* ic, const float* is, float* vel,
                    cudaStream_t s) {
+  d->cur_slot = slot;
   const int n_text = mode == kImage ? 0 : L;
   const int n_img = mode == kText ? 0 : N;
   const int R = n_text + n_img;
@@ -401,6 +406,8 @@ size_t qi_kv_cache_bytes(int blocks, int L) {
 qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out) {
   if (!cfg || !out) return fail(QI_ERR_INVALID_ARG, "qi_dit_create: NULL argument");
   *out = nullptr;
+  if (cfg->kv_slots < 0 || cfg->kv_slots > 2)
+    return fail(QI_ERR_SHAPE, "qi_dit_create: kv_slots %d (0, 1 or 2)", cfg->kv_slots);
   if (cfg->blocks < 1 || cfg->blocks > QI_BLOCKS || cfg->L_max < QI_L_MIN || cfg->L_max > QI_L_MAX ||
       cfg->N_max < QI_N_MIN || cfg->N_max > QI_N_MAX)
     return fail(QI_ERR_SHAPE, "qi_dit_create: blocks %d L_max %d N_max %d out of range", cfg->blocks, cfg->L_max,
@@ -412,6 +419,7 @@ qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out) {
   d->L_max = cfg->L_max;
   d->N_max = cfg->N_max;
   d->R_max = cfg->L_max + cfg->N_max;
+  d->slots = cfg->kv_slots == 2 ? 2 : 1;
   d->loaded_block.assign(cfg->blocks, false);
   cudaDeviceGetAttribute(&d->num_sms, cudaDevAttrMultiProcessorCount, device);
 
@@ -465,7 +473,9 @@ qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out) {
       {(void**)&d->txt_a, (size_t)d->L_max * kHidden * 2}, {(void**)&d->temb_e, 2 * kTdim * 4},
       {(void**)&d->temb_h, 2 * kHidden * 4}, {(void**)&d->temb, 2 * kHidden * 4},
       {(void**)&d->mod, 2 * (size_t)kMod * 4}, {(void**)&d->err, 256}, {(void**)&d->ovf, 256},
-      {(void**)&d->kv, (size_t)cfg->blocks * 2 * R * kHidden * 2},
+      {(void**)&d->kv, (size_t)d->slots * cfg->blocks * 2 * R * kHidden * 2},
+      {(void**)&d->vel_pos, d->slots == 2 ? (size_t)d->N_max * kPatch * 4 : 0},
+      {(void**)&d->vel_neg, d->slots == 2 ? (size_t)d->N_max * kPatch * 4 : 0},
   };
   size_t abytes = 0;
   for (auto& s : asegs) abytes += align_up(s.bytes, 1024);
@@ -656,8 +666,8 @@ qi_status qi_dit_step(qi_dit* d, const float* img_tokens, int N, const float* tx
   if (!img_tokens || !img_cos || !img_sin || !vel) return fail(QI_ERR_INVALID_ARG, "qi_dit_step: NULL image tensor");
   if (!use_cache && (!txt_feats || !txt_cos || !txt_sin))
     return fail(QI_ERR_INVALID_ARG, "qi_dit_step: joint pass needs txt_feats and txt_cos/txt_sin");
-  if (use_cache && d->cache_L != L)
-    return fail(QI_ERR_STATE, "qi_dit_step: USE_CACHE but the text K/V capture is for L=%d, not %d", d->cache_L, L);
+  if (use_cache && d->cache_L[0] != L)
+    return fail(QI_ERR_STATE, "qi_dit_step: USE_CACHE but the text K/V capture is for L=%d, not %d", d->cache_L[0], L);
   if (!all_loaded(d)) return fail(QI_ERR_STATE, "qi_dit_step: weights not loaded");
   if (!std::isfinite(timestep)) return fail(QI_ERR_INVALID_ARG, "qi_dit_step: timestep not finite");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -682,15 +692,56 @@ qi_status qi_dit_step(qi_dit* d, const float* img_tokens, int N, const float* tx
       QI_CUDA(cudaMemcpyAsync(d->st_tc, txt_cos, (size_t)L * kRopeCols * 4, h2d, s));
       QI_CUDA(cudaMemcpyAsync(d->st_ts, txt_sin, (size_t)L * kRopeCols * 4, h2d, s));
     }
-    QI_TRY(run_pass(d, use_cache ? kImage : kJoint, d->st_img, N, d->st_txt, L, timestep, d->st_tc, d->st_ts,
+    QI_TRY(run_pass(d, 0, use_cache ? kImage : kJoint, d->st_img, N, d->st_txt, L, timestep, d->st_tc, d->st_ts,
                     d->st_ic, d->st_is, d->st_vel, s));
     QI_CUDA(cudaMemcpyAsync(vel, d->st_vel, (size_t)N * kPatch * 4, cudaMemcpyDeviceToHost, s));
-    if (!use_cache) d->cache_L = L;
+    if (!use_cache) d->cache_L[0] = L;
     return check_device_word(d, s);
   }
-  QI_TRY(run_pass(d, use_cache ? kImage : kJoint, img_tokens, N, txt_feats, L, timestep, txt_cos, txt_sin, img_cos,
-                  img_sin, vel, s));
-  if (!use_cache) d->cache_L = L;
+  QI_TRY(run_pass(d, 0, use_cache ? kImage : kJoint, img_tokens, N, txt_feats, L, timestep, txt_cos, txt_sin,
+                  img_cos, img_sin, vel, s));
+  if (!use_cache) d->cache_L[0] = L;
+  return QI_OK;
+}
+
+qi_status qi_dit_step_cfg(qi_dit* d, const float* img_tokens, int N, float timestep, float guidance,
+                          const float* pos_feats, int L_pos, const float* pos_txt_cos, const float* pos_txt_sin,
+                          const float* pos_img_cos, const float* pos_img_sin, const float* neg_feats, int L_neg,
+                          const float* neg_txt_cos, const float* neg_txt_sin, const float* neg_img_cos,
+                          const float* neg_img_sin, float* vel, unsigned flags, qi_stream_t stream) {
+  if (!d) return fail(QI_ERR_INVALID_ARG, "qi_dit_step_cfg: NULL handle");
+  if (flags & ~QI_STEP_USE_CACHE) return fail(QI_ERR_INVALID_ARG, "qi_dit_step_cfg: flags %u", flags);
+  if (d->slots != 2) return fail(QI_ERR_STATE, "qi_dit_step_cfg: the handle was created with one K/V slot");
+  const bool use_cache = flags & QI_STEP_USE_CACHE;
+  if (N < QI_N_MIN || N > d->N_max || L_pos < QI_L_MIN || L_pos > d->L_max || L_neg < QI_L_MIN || L_neg > d->L_max)
+    return fail(QI_ERR_SHAPE, "qi_dit_step_cfg: N %d L_pos %d L_neg %d (max %d, %d)", N, L_pos, L_neg, d->N_max,
+                d->L_max);
+  if (!img_tokens || !vel || !pos_img_cos || !pos_img_sin || !neg_img_cos || !neg_img_sin)
+    return fail(QI_ERR_INVALID_ARG, "qi_dit_step_cfg: NULL image tensor");
+  if (!use_cache && (!pos_feats || !pos_txt_cos || !pos_txt_sin || !neg_feats || !neg_txt_cos || !neg_txt_sin))
+    return fail(QI_ERR_INVALID_ARG, "qi_dit_step_cfg: a joint pass needs both prompts and their tables");
+  if (use_cache && (d->cache_L[0] != L_pos || d->cache_L[1] != L_neg))
+    return fail(QI_ERR_STATE, "qi_dit_step_cfg: USE_CACHE but the captures are for L=%d/%d, not %d/%d", d->cache_L[0],
+                d->cache_L[1], L_pos, L_neg);
+  if (!all_loaded(d)) return fail(QI_ERR_STATE, "qi_dit_step_cfg: weights not loaded");
+  if (!std::isfinite(timestep) || !std::isfinite(guidance))
+    return fail(QI_ERR_INVALID_ARG, "qi_dit_step_cfg: timestep or guidance not finite");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  QI_CUDA(cudaSetDevice(d->device));
+  const PassMode mode = use_cache ? kImage : kJoint;
+  QI_TRY(run_pass(d, 0, mode, img_tokens, N, pos_feats, L_pos, timestep, pos_txt_cos, pos_txt_sin, pos_img_cos,
+                  pos_img_sin, d->vel_pos, s));
+  QI_TRY(run_pass(d, 1, mode, img_tokens, N, neg_feats, L_neg, timestep, neg_txt_cos, neg_txt_sin, neg_img_cos,
+                  neg_img_sin, d->vel_neg, s));
+  d->cur_slot = 0;
+  {
+    ProfScope ps(d, s, 5);
+    QI_CUDA(qi::launch_cfg_combine(d->vel_pos, d->vel_neg, guidance, vel, static_cast<long long>(N) * kPatch, s));
+  }
+  if (!use_cache) {
+    d->cache_L[0] = L_pos;
+    d->cache_L[1] = L_neg;
+  }
   return QI_OK;
 }
 
@@ -701,8 +752,8 @@ qi_status qi_text_kv_capture(qi_dit* d, const float* txt_feats, int L, const flo
   if (!all_loaded(d)) return fail(QI_ERR_STATE, "qi_text_kv_capture: weights not loaded");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   QI_CUDA(cudaSetDevice(d->device));
-  QI_TRY(run_pass(d, kText, nullptr, 0, txt_feats, L, 0.f, txt_cos, txt_sin, nullptr, nullptr, nullptr, s));
-  d->cache_L = L;
+  QI_TRY(run_pass(d, 0, kText, nullptr, 0, txt_feats, L, 0.f, txt_cos, txt_sin, nullptr, nullptr, nullptr, s));
+  d->cache_L[0] = L;
   return QI_OK;
 }
 
@@ -724,6 +775,7 @@ qi_status qi_dit_block_forward(qi_dit* d, int block, float* hidden, int L, int N
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   QI_CUDA(cudaSetDevice(d->device));
   const int R = L + N;
+  d->cur_slot = 0;
   QI_CUDA(cudaMemcpyAsync(d->x, hidden, (size_t)R * kHidden * 4, cudaMemcpyDeviceToDevice, s));
   QI_TRY(compute_mod(d, t_img, s));
   QI_CUDA(qi::launch_block_prep(d->x, R, L, d->mod, d->xa, d->ssp, s));
@@ -741,6 +793,7 @@ qi_status qi_dit_read_kv(qi_dit* d, int block, int row0, int rows, uint16_t* k_o
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   QI_CUDA(cudaSetDevice(d->device));
   const size_t bytes = (size_t)rows * kHidden * 2;
+  d->cur_slot = 0;
   QI_CUDA(cudaMemcpyAsync(k_out, d->k_of(block) + (size_t)row0 * kHidden, bytes, cudaMemcpyDeviceToDevice, s));
   QI_CUDA(cudaMemcpyAsync(v_out, d->v_of(block) + (size_t)row0 * kHidden, bytes, cudaMemcpyDeviceToDevice, s));
   return QI_OK;

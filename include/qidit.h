@@ -93,6 +93,8 @@ typedef struct qi_dit_config {
   int blocks; /* 1..32 (32 for the real model; fewer for tests)                 */
   int L_max;  /* largest prompt length this handle serves (1..512)              */
   int N_max;  /* largest image token count this handle serves (1..16384)        */
+  int kv_slots; /* text K/V slots: 0 or 1 = one; 2 = a second slot for the negative
+                 * prompt of classifier-free guidance (qi_dit_step_cfg)          */
 } qi_dit_config;
 
 /* Global (non-block) tensors, bf16 bits, [out, in] row-major. */
@@ -215,6 +217,24 @@ qi_status qi_dit_step(qi_dit* dit, const float* img_tokens, int N, const float* 
                       float timestep, const float* txt_cos, const float* txt_sin,
                       const float* img_cos, const float* img_sin, float* vel, unsigned flags,
                       qi_stream_t stream);
+
+/* Classifier-free guidance step [MLX page, "Optional modes": the negative
+ * prompt is used as noise = neg + g * (pos - neg), with its K/V in a second
+ * slot ("Text K/V reuse")]. Runs the pass of qi_dit_step for the conditional
+ * prompt (K/V slot 0) and for the negative prompt (slot 1) on the same
+ * img_tokens and timestep, then vel = neg + guidance * (pos - neg) in float32,
+ * each operation rounded on its own. Each prompt has its own tables: image
+ * positions carry the prompt length in their frame coordinate.
+ * flags = QI_STEP_JOINT: both passes are joint and capture their slot.
+ * flags = QI_STEP_USE_CACHE: image rows only; the *_feats and *_txt_* tensors
+ * may be NULL; the captures must be for L_pos and L_neg.
+ * Errors: STATE (handle created with kv_slots != 2, no matching capture),
+ * SHAPE, INVALID_ARG, CUDA. */
+qi_status qi_dit_step_cfg(qi_dit* dit, const float* img_tokens, int N, float timestep, float guidance,
+                          const float* pos_feats, int L_pos, const float* pos_txt_cos, const float* pos_txt_sin,
+                          const float* pos_img_cos, const float* pos_img_sin, const float* neg_feats, int L_neg,
+                          const float* neg_txt_cos, const float* neg_txt_sin, const float* neg_img_cos,
+                          const float* neg_img_sin, float* vel, unsigned flags, qi_stream_t stream);
 
 /* Text-only pass [REUSE]: run the L text rows (t = 0 modulation, causal over
  * text) through every block and store their K/V, the same values a joint pass

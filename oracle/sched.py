@@ -67,3 +67,15 @@ def euler_update(x: np.ndarray, vel: np.ndarray, sigma_i, sigma_next) -> np.ndar
     dt = np.float32(np.float32(sigma_next) - np.float32(sigma_i))
     prod = (np.asarray(vel, np.float32) * dt).astype(np.float32)
     return (np.asarray(x, np.float32) + prod).astype(np.float32)
+
+
+def cfg_combine(pos: np.ndarray, neg: np.ndarray, g) -> np.ndarray:
+    """Classifier-free guidance: neg + g * (pos - neg), float32, each operation rounded.
+
+    Source: MLX page, "Optional modes (approximate or slower)": true CFG uses the
+    negative prompt as noise = neg + g * (pos - neg).
+    """
+    pos = np.asarray(pos, np.float32)
+    neg = np.asarray(neg, np.float32)
+    d = (pos - neg).astype(np.float32)
+    return (neg + (np.float32(g) * d).astype(np.float32)).astype(np.float32)

@@ -95,3 +95,12 @@ def test_status_codes(qi):
     assert L.qi_euler_update(None, None, 8, 1.0, 0.5, None) == 1
     assert L.qi_dit_step(None, None, 8, None, 8, 0.5, None, None, None, None, None, 0, None) == 1
     assert L.qi_attention_f16(None, None, None, None, 1, 0, 1, 1, None) == 1
+
+
+def test_kv_slots_range(qi):
+    L = qi.lib()
+    h = ctypes.c_void_p()
+    assert L.qi_dit_create(ctypes.byref(qi.DitConfig(1, 8, 64, 3)), 0, ctypes.byref(h)) == 2
+    assert L.qi_dit_create(ctypes.byref(qi.DitConfig(1, 8, 64, -1)), 0, ctypes.byref(h)) == 2
+    assert L.qi_dit_step_cfg(None, None, 64, 0.5, 2.0, None, 8, None, None, None, None, None, 8, None, None,
+                             None, None, None, 0, None) == 1

@@ -113,3 +113,22 @@ def test_euler_telescopes():
     for i in range(40):
         x = sched.euler_update(x, c, s[i], s[i + 1])
     assert np.allclose(x, -c, rtol=0, atol=1e-5)
+
+
+def test_cfg_combine_closed_forms():
+    rng = np.random.default_rng(4)
+    pos = rng.standard_normal(500).astype(np.float32)
+    neg = rng.standard_normal(500).astype(np.float32)
+    # g = 0 returns the negative branch exactly; g = 1 the conditional one to within rounding
+    assert np.array_equal(sched.cfg_combine(pos, neg, 0.0), neg)
+    assert np.allclose(sched.cfg_combine(pos, neg, 1.0), pos, rtol=0, atol=1e-6)
+    # equal branches are a fixed point for any g
+    assert np.array_equal(sched.cfg_combine(pos, pos, 4.5), pos)
+    # affine in g: the midpoint of g = 1 and g = 3 is g = 2
+    a, b, c = (sched.cfg_combine(pos, neg, gg).astype(np.float64) for gg in (1.0, 2.0, 3.0))
+    assert np.allclose((a + c) / 2, b, rtol=0, atol=1e-5)
+    # the stated order of operations, element by element in float64 with explicit rounding
+    for i in range(0, 500, 53):
+        d = np.float32(float(pos[i]) - float(neg[i]))
+        m = np.float32(float(np.float32(2.5)) * float(d))
+        assert sched.cfg_combine(pos[i:i + 1], neg[i:i + 1], 2.5)[0] == np.float32(float(neg[i]) + float(m))
