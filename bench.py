@@ -223,7 +223,7 @@ def run_ours(args, rank, world, local_rank):
     qi.build()
     stream = torch.cuda.current_stream()
 
-    dit = qi.DiT(blocks=BLOCKS, L_max=L, N_max=N, device=local_rank)
+    dit = qi.DiT(blocks=BLOCKS, L_max=L, N_max=N, device=local_rank, kv_slots=2)
     gpu_weights(dit, CASE.seed * 1000 + rank, dev)
 
     sig, ts = qi.flow_sigmas(STEPS_PER_IMAGE, N)
@@ -289,6 +289,27 @@ def run_ours(args, rank, world, local_rank):
     flops = njoint * step_flops(True) + nimg * step_flops(False)
     value = world * args.steps / (ms / 1e3)
     tflops = world * flops / (ms / 1e3) / 1e12
+
+    # ---- classifier-free guidance (second K/V slot): a 9-token negative prompt (the
+    # host contract's empty-prompt template), guidance 2.5; 1 joint + CFG_STEPS - 1 cached
+    CFG_STEPS, L_NEG, GUIDE = 10, 9, 2.5
+    neg_txt = torch.randn(L_NEG, HIDDEN, generator=g, device=dev)
+    ntc, nts, nic, nis = qi.rope_tables(L_NEG, H, W_)
+    pos_p = dict(feats=txt, L=L, txt_cos=tc, txt_sin=tsn, img_cos=ic, img_sin=isn)
+    neg_p = dict(feats=neg_txt, L=L_NEG, txt_cos=ntc, txt_sin=nts, img_cos=nic, img_sin=nis)
+    x.copy_(x0)
+    dit.step_cfg(x, tvals[0], GUIDE, pos_p, neg_p, vel=vel)  # warm-up
+    torch.cuda.synchronize()
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for i in range(CFG_STEPS):
+        dit.step_cfg(x, tvals[i], GUIDE, pos_p, neg_p, use_cache=i > 0, vel=vel)
+        qi.euler_update(x, vel, float(sig[i]), float(sig[i + 1]))
+    c1.record(stream)
+    torch.cuda.synchronize()
+    dit.check()
+    cfg_ms = c0.elapsed_time(c1) / CFG_STEPS
 
     # ---- end to end through the public API with host buffers
     xh = torch.empty(N, 64, dtype=torch.float32).pin_memory()
@@ -363,6 +384,9 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": world * e2e_steps / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": h2d / e2e_steps,
                 "d2h_bytes_per_step": d2h / e2e_steps},
         "clocks": clk,
+        "cfg": {"steps_per_s": world * 1e3 / cfg_ms, "ms_per_step": cfg_ms, "guidance": GUIDE, "neg_tokens": L_NEG,
+                "steps": CFG_STEPS, "note": "two passes per step (conditional + negative prompt), 1 joint + "
+                                            f"{CFG_STEPS - 1} image-only"},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         times = oracle_block_sample(9)
