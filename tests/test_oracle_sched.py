@@ -132,3 +132,121 @@ def test_cfg_combine_closed_forms():
         d = np.float32(float(pos[i]) - float(neg[i]))
         m = np.float32(float(np.float32(2.5)) * float(d))
         assert sched.cfg_combine(pos[i:i + 1], neg[i:i + 1], 2.5)[0] == np.float32(float(neg[i]) + float(m))
+
+
+# ----------------------------------------------------------------------------- DPM++ 2M
+
+def _gaussian_velocity(m, s):
+    """Exact flow-matching velocity when every coordinate of x0 is N(m, s^2):
+    D(x, sigma) = E[x0 | x_sigma = x] in closed form, v = (x - D) / sigma."""
+    def vel(x, sg):
+        sg = float(sg)
+        gain = (1 - sg) * s * s / ((1 - sg) ** 2 * s * s + sg * sg)
+        D = m + gain * (x.astype(np.float64) - (1 - sg) * m)
+        return ((x - D) / sg).astype(np.float32)
+    return vel
+
+
+def test_dpmpp2m_point_mass_stays_on_the_path():
+    """With all data at one point x0, v = (x - x0) / sigma and D = x0 at every step: the
+    exponential integrator is then exact, so x stays on (1 - sigma) x0 + sigma eps and
+    the last step lands on x0."""
+    rng = np.random.default_rng(7)
+    x0 = rng.standard_normal(4096).astype(np.float32)
+    eps = rng.standard_normal(4096).astype(np.float32)
+    sig, _ = sched.flow_sigmas(40, 4096)
+    x, dp = eps.copy(), None
+    for i in range(40):
+        v = ((x.astype(np.float64) - x0) / float(sig[i])).astype(np.float32)
+        x, dp = sched.dpmpp2m_update(x, v, dp, sig, i)
+        s = float(sig[i + 1])
+        on_path = (1 - s) * x0.astype(np.float64) + s * eps.astype(np.float64)
+        assert np.abs(x - on_path).max() < 2e-5, i
+    assert np.abs(x - x0).max() < 2e-6
+
+
+def test_dpmpp2m_first_order_step_is_euler():
+    """alpha = 1 - sigma makes the first-order step x + (sigma_{i+1} - sigma_i) v."""
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal(1 << 14).astype(np.float32)
+    v = rng.standard_normal(1 << 14).astype(np.float32)
+    sig, _ = sched.flow_sigmas(40, 1024)
+    order, a, b, c0, c1 = sched.dpmpp2m_coeffs(sig, 0)
+    assert order == 1 and abs(float(a) + float(b) - 1.0) < 1e-7
+    got, D = sched.dpmpp2m_update(x, v, None, sig, 0)
+    ref = x.astype(np.float64) + (float(sig[1]) - float(sig[0])) * v.astype(np.float64)
+    assert np.abs(got - ref).max() < 4e-6 * (1 + np.abs(ref).max())
+    assert np.array_equal(D, (x - (sig[0] * v).astype(np.float32)).astype(np.float32))
+
+
+def test_dpmpp2m_correction_is_the_lambda_midpoint():
+    """The 2M data estimate extrapolates D linearly in lambda through the last two
+    evaluations to the middle of the step, lambda_i + h_i / 2."""
+    sig, _ = sched.flow_sigmas(40, 4096)
+    for i in (2, 5, 17, 38):
+        order, a, b, c0, c1 = sched.dpmpp2m_coeffs(sig, i)
+        assert order == 2
+        lp, l0, ln = (sched.half_log_snr(sig[j]) for j in (i - 1, i, i + 1))
+        A, B = 0.3, -1.7                           # D(lambda) = A + B lambda
+        D_prev, D_i = A + B * lp, A + B * l0
+        mid = A + B * (l0 + (ln - l0) / 2)
+        assert abs(float(c0) * D_i - float(c1) * D_prev - mid) < 1e-6 * (1 + abs(mid))
+        assert abs(float(c0) - 1.0 - float(c1)) <= np.spacing(np.float32(c0))  # each rounded once from float64
+
+
+def test_dpmpp2m_is_second_order():
+    """Gaussian data (exact ODE solution known): the error at sigma = 0.02 falls ~4x per
+    doubling of the step count; Euler's falls ~2x."""
+    m, s = 0.7, 1.3
+    vel = _gaussian_velocity(m, s)
+    z = np.random.default_rng(0).standard_normal(20000).astype(np.float32)
+
+    def err(steps, dpm):
+        sig, _ = sched.flow_sigmas(steps, 4096)
+        sig = sig[:-1]                             # stop at the terminal sigma 0.02
+        x, dp = z.copy(), None
+        for i in range(len(sig) - 1):
+            v = vel(x, sig[i])
+            if dpm:
+                x, dp = sched.dpmpp2m_update(x, v, dp, sig, i)
+            else:
+                x = sched.euler_update(x, v, sig[i], sig[i + 1])
+        se = float(sig[-1])
+        exact = (1 - se) * m + math.sqrt((1 - se) ** 2 * s * s + se * se) * z.astype(np.float64)
+        return np.abs(x - exact).max()
+
+    e = [err(n, True) for n in (20, 40, 80)]
+    for k in range(2):
+        assert 3.6 < e[k] / e[k + 1] < 6.0, e
+    eu = [err(n, False) for n in (40, 80)]
+    assert 1.8 < eu[0] / eu[1] < 2.2 and e[1] < eu[0] / 4
+
+
+def test_dpmpp2m_step_kinds():
+    sig, _ = sched.flow_sigmas(40, 4096)
+    assert sched.dpmpp2m_coeffs(sig, 0)[0] == 1            # no previous D
+    assert sched.dpmpp2m_coeffs(sig, 1)[0] == 1            # previous sigma is 1: lambda = -inf
+    assert sched.dpmpp2m_coeffs(sig, 2)[0] == 2
+    assert sched.dpmpp2m_coeffs(sig, 39)[0] == 0           # sigma_40 = 0
+    x = np.array([1.0, -2.0, 3.0], np.float32)
+    v = np.array([0.5, 0.25, -1.0], np.float32)
+    xn, D = sched.dpmpp2m_update(x, v, None, sig, 39)
+    assert np.array_equal(xn, D) and np.array_equal(D, (x - (sig[39] * v).astype(np.float32)).astype(np.float32))
+    # a schedule that does not start at 1 still takes a first-order first step
+    s2 = np.array([0.9, 0.5, 0.2, 0.0], np.float32)
+    assert [sched.dpmpp2m_coeffs(s2, i)[0] for i in range(3)] == [1, 2, 0]
+    assert sched.half_log_snr(1.0) == -math.inf and sched.half_log_snr(0.0) == math.inf
+    assert sched.half_log_snr(0.5) == 0.0
+
+
+def test_dpmpp2m_midpoint_pin_rejects_an_inverted_ratio():
+    """Control: 1/(2r) written with r inverted (h_i / h_{i-1} in place of h_{i-1} / h_i)
+    still converges at second order, so only the midpoint pin can catch it."""
+    sig, _ = sched.flow_sigmas(40, 4096)
+    i = 5
+    lp, l0, ln = (sched.half_log_snr(sig[j]) for j in (i - 1, i, i + 1))
+    wrong_c1 = (l0 - lp) / (2 * (ln - l0))
+    A, B = 0.3, -1.7
+    D_prev, D_i = A + B * lp, A + B * l0
+    mid = A + B * (l0 + (ln - l0) / 2)
+    assert abs((1 + wrong_c1) * D_i - wrong_c1 * D_prev - mid) > 1e-3
