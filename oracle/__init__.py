@@ -8,9 +8,11 @@ which draws seeded inputs and weights and holds none of the model's arithmetic.
 Modules
 -------
 rope       3-axis RoPE tables, token positions, noise packing (host contract s4-5)
-sched      FlowMatch Euler sigmas, timesteps, Euler update (host contract s6)
+sched      FlowMatch Euler sigmas, timesteps, Euler update (host contract s6),
+           guidance combine and the DPM++ 2M step (MLX page, optional modes)
 attention  block-causal attention: masked dense, two-segment, brute force
 dit        timestep embedding, shared modulation, block, full DiT, output head
+fbcache    first-block cache ("Fast mode") around the DiT pass (MLX page)
 
 Everything is numpy float32 (bf16 weights widened exactly); the brute-force
 checkers use Python float64 loops on tiny shapes.
