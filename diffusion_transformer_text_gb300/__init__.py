@@ -39,7 +39,7 @@ SYMBOLS = (
     "qi_dit_step", "qi_text_kv_capture", "qi_kv_cache_bytes", "qi_dit_check",
     "qi_dit_block_forward", "qi_dit_read_kv", "qi_dit_set_trace", "qi_dit_profile",
     "qi_dit_profile_read", "qi_last_error", "qi_gemm_bf16", "qi_attention_f16", "qi_gemm_bf16_noalloc",
-    "qi_dit_step_cfg",
+    "qi_dit_step_cfg", "qi_dpmpp2m_coeffs", "qi_dpmpp2m_update", "qi_dit_step_fbcache", "qi_dit_fbcache_reset",
 )
 
 
@@ -106,6 +106,10 @@ def lib() -> ctypes.CDLL:
         "qi_attention_f16": [P, P, P, P, I, I, I, I, P],
         "qi_gemm_bf16_noalloc": [P, P, P, I, I, I, I, P],
         "qi_dit_step_cfg": [P, P, I, F, F, P, I, P, P, P, P, P, I, P, P, P, P, P, U, P],
+        "qi_dpmpp2m_coeffs": [P, I, I, P, P],
+        "qi_dit_step_fbcache": [P, P, I, P, I, F, P, P, P, P, F, P, P, P, U, P],
+        "qi_dit_fbcache_reset": [P],
+        "qi_dpmpp2m_update": [P, P, P, I, P, I, I, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -199,6 +203,33 @@ def euler_update(x, vel, sigma_i: float, sigma_next: float):
     _dev_f32(x, (N, PATCH), "x")
     _dev_f32(vel, (N, PATCH), "vel")
     _check(lib().qi_euler_update(_ptr(x), _ptr(vel), N, sigma_i, sigma_next, _stream()))
+    return x
+
+
+def _host_sigmas(sigmas):
+    import numpy as np
+    s = np.ascontiguousarray(np.asarray(sigmas, dtype=np.float32))
+    return s, s.ctypes.data_as(ctypes.c_void_p)
+
+
+def dpmpp2m_coeffs(sigmas, i: int):
+    """Host-side coefficients of DPM++ 2M step i: (order, a, b, c0, c1) as float32 values."""
+    import numpy as np
+    s, sp = _host_sigmas(sigmas)
+    order = ctypes.c_int(-1)
+    c = np.zeros(4, np.float32)
+    _check(lib().qi_dpmpp2m_coeffs(sp, len(s) - 1, i, ctypes.byref(order), c.ctypes.data_as(ctypes.c_void_p)))
+    return (order.value, *[np.float32(v) for v in c])
+
+
+def dpmpp2m_update(x, vel, d_prev, sigmas, i: int):
+    """In place: DPM++ 2M step i on x [N, 64]; d_prev [N, 64] carries D between steps."""
+    N = x.shape[0]
+    _dev_f32(x, (N, PATCH), "x")
+    _dev_f32(vel, (N, PATCH), "vel")
+    _dev_f32(d_prev, (N, PATCH), "d_prev")
+    s, sp = _host_sigmas(sigmas)
+    _check(lib().qi_dpmpp2m_update(_ptr(x), _ptr(vel), _ptr(d_prev), N, sp, len(s) - 1, i, _stream()))
     return x
 
 
@@ -327,6 +358,33 @@ class DiT:
             _ptr(neg["img_cos"]), _ptr(neg["img_sin"]), _ptr(vel), STEP_USE_CACHE if use_cache else STEP_JOINT,
             _stream(stream)))
         return vel
+
+    def step_fbcache(self, img_tokens, txt_feats, L: int, timestep: float, txt_cos, txt_sin, img_cos, img_sin,
+                     threshold: float, use_cache: bool = False, vel=None, stream=None):
+        """One step under the first-block cache (txt_* may be None with use_cache).
+        Returns (vel, rel_change, skipped)."""
+        import torch
+        N = img_tokens.shape[0]
+        _dev_f32(img_tokens, (N, PATCH), "img_tokens")
+        _dev_f32(img_cos, (N, ROPE_COLS), "img_cos")
+        _dev_f32(img_sin, (N, ROPE_COLS), "img_sin")
+        if not use_cache:
+            _dev_f32(txt_feats, (L, HIDDEN), "txt_feats")
+            _dev_f32(txt_cos, (L, ROPE_COLS), "txt_cos")
+            _dev_f32(txt_sin, (L, ROPE_COLS), "txt_sin")
+        if vel is None:
+            vel = torch.empty(N, PATCH, device=img_tokens.device, dtype=torch.float32)
+        rel = ctypes.c_float(0.0)
+        skipped = ctypes.c_int(-1)
+        _check(lib().qi_dit_step_fbcache(
+            self._h, _ptr(img_tokens), N, None if use_cache else _ptr(txt_feats), L, float(timestep),
+            None if use_cache else _ptr(txt_cos), None if use_cache else _ptr(txt_sin), _ptr(img_cos),
+            _ptr(img_sin), float(threshold), _ptr(vel), ctypes.byref(rel), ctypes.byref(skipped),
+            STEP_USE_CACHE if use_cache else STEP_JOINT, _stream(stream)))
+        return vel, rel.value, bool(skipped.value)
+
+    def fbcache_reset(self):
+        _check(lib().qi_dit_fbcache_reset(self._h))
 
     def text_kv_capture(self, txt_feats, txt_cos, txt_sin, stream=None):
         L = txt_feats.shape[0]

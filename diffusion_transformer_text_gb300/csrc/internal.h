@@ -114,11 +114,21 @@ cudaError_t launch_head(const float* x, int N, const float* ssp, const uint16_t*
 cudaError_t launch_block_prep(const float* x, int R, int n_text, const float* mod, act_t* xa, float* ssp,
                               cudaStream_t s);
 cudaError_t launch_euler(float* x, const float* vel, long long n, float s_i, float s_next, cudaStream_t s);
+cudaError_t launch_dpmpp2m(float* x, const float* vel, float* dprev, long long n, float sigma_i, int order, float a,
+                           float b, float c0, float c1, cudaStream_t s);
 cudaError_t launch_rope_axis(float theta, float* c0, float* s0, float* c1, float* s1, float* c2, float* s2,
                              cudaStream_t s);
 cudaError_t launch_rope_tokens(int L, int h, int w, float theta, float* tc, float* ts, float* ic, float* is,
                                cudaStream_t s);
 cudaError_t launch_pack_noise(const float* z, int h, int w, float* x, cudaStream_t s);
+// First-block cache. residual: r0 = x1 - x0 and x1c = x1 over rows x 4096; when ref is
+// not null also out = {sum |r0 - ref|, sum |ref|} (double), via `grid` partials.
+cudaError_t launch_fbc_residual(const float* x1, const float* x0, const float* ref, float* r0, float* x1c, int rows,
+                                int grid, double2* partial, double* out, cudaStream_t s);
+// x += rest and the per-row sum-of-squares partials of the result.
+cudaError_t launch_fbc_apply(float* x, const float* rest, float* ssp, int rows, cudaStream_t s);
+// rest = xl - x1c.
+cudaError_t launch_fbc_rest(const float* xl, const float* x1c, float* rest, int rows, int grid, cudaStream_t s);
 // Classifier-free guidance: out = neg + g * (pos - neg), each operation rounded
 // on its own (no FMA contraction).
 cudaError_t launch_cfg_combine(const float* pos, const float* neg, float g, float* out, long long n, cudaStream_t s);

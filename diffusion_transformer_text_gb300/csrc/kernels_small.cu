@@ -348,6 +348,140 @@ __global__ void cfg_combine_kernel(const float* __restrict__ pos, const float* _
   if (i < n) out[i] = __fadd_rn(neg[i], __fmul_rn(g, __fsub_rn(pos[i], neg[i])));
 }
 
+// DPM++ 2M step (float32, no contraction): D = x - sigma_i v; order 2 blends D with
+// the previous step's D; order 0 returns D. D is kept for the next step.
+__device__ __forceinline__ float dpm_one(float x, float v, float& dp, float sigma_i, int order, float a, float b,
+                                         float c0, float c1) {
+  const float D = __fsub_rn(x, __fmul_rn(sigma_i, v));
+  float Dm = D;
+  if (order == 2) Dm = __fsub_rn(__fmul_rn(c0, D), __fmul_rn(c1, dp));
+  dp = D;
+  return order == 0 ? D : __fadd_rn(__fmul_rn(a, x), __fmul_rn(b, Dm));
+}
+
+__global__ void dpmpp2m_kernel(float* __restrict__ x, const float* __restrict__ vel, float* __restrict__ dprev,
+                               long long n, float sigma_i, int order, float a, float b, float c0, float c1) {
+  const long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+  if (i + 3 < n) {
+    float4 xv = *reinterpret_cast<float4*>(x + i);
+    const float4 v = *reinterpret_cast<const float4*>(vel + i);
+    float4 dp = order == 2 ? *reinterpret_cast<const float4*>(dprev + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    xv.x = dpm_one(xv.x, v.x, dp.x, sigma_i, order, a, b, c0, c1);
+    xv.y = dpm_one(xv.y, v.y, dp.y, sigma_i, order, a, b, c0, c1);
+    xv.z = dpm_one(xv.z, v.z, dp.z, sigma_i, order, a, b, c0, c1);
+    xv.w = dpm_one(xv.w, v.w, dp.w, sigma_i, order, a, b, c0, c1);
+    *reinterpret_cast<float4*>(x + i) = xv;
+    *reinterpret_cast<float4*>(dprev + i) = dp;
+  } else {
+    for (long long j = i; j < n; ++j) {
+      float dp = order == 2 ? dprev[j] : 0.f;
+      x[j] = dpm_one(x[j], vel[j], dp, sigma_i, order, a, b, c0, c1);
+      dprev[j] = dp;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- first-block cache
+
+// r0 = x1 - x0 (block 0's residual), copies x1, and (when ref != nullptr) per-CTA sums
+// of |r0 - ref| and |ref|: float within a thread, double across the CTA.
+constexpr int kFbcThreads = 256;
+__global__ void __launch_bounds__(kFbcThreads) fbc_residual_kernel(const float* __restrict__ x1,
+                                                                   const float* __restrict__ x0,
+                                                                   const float* __restrict__ ref,
+                                                                   float* __restrict__ r0, float* __restrict__ x1c,
+                                                                   long long n4, double2* __restrict__ partial) {
+  float num = 0.f, den = 0.f;
+  const long long stride = static_cast<long long>(gridDim.x) * kFbcThreads;
+  for (long long i = static_cast<long long>(blockIdx.x) * kFbcThreads + threadIdx.x; i < n4; i += stride) {
+    const float4 a = reinterpret_cast<const float4*>(x1)[i];
+    const float4 b = reinterpret_cast<const float4*>(x0)[i];
+    const float4 r = make_float4(__fsub_rn(a.x, b.x), __fsub_rn(a.y, b.y), __fsub_rn(a.z, b.z), __fsub_rn(a.w, b.w));
+    reinterpret_cast<float4*>(r0)[i] = r;
+    reinterpret_cast<float4*>(x1c)[i] = a;
+    if (ref) {
+      const float4 p = reinterpret_cast<const float4*>(ref)[i];
+      num += fabsf(r.x - p.x) + fabsf(r.y - p.y) + fabsf(r.z - p.z) + fabsf(r.w - p.w);
+      den += fabsf(p.x) + fabsf(p.y) + fabsf(p.z) + fabsf(p.w);
+    }
+  }
+  if (!ref) return;
+  __shared__ double sn[kFbcThreads], sd[kFbcThreads];
+  sn[threadIdx.x] = num;
+  sd[threadIdx.x] = den;
+  __syncthreads();
+  for (int o = kFbcThreads / 2; o > 0; o >>= 1) {
+    if (threadIdx.x < o) {
+      sn[threadIdx.x] += sn[threadIdx.x + o];
+      sd[threadIdx.x] += sd[threadIdx.x + o];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) partial[blockIdx.x] = make_double2(sn[0], sd[0]);
+}
+
+// Sums the per-CTA partials in a fixed order: out = {sum |r0 - ref|, sum |ref|}.
+__global__ void __launch_bounds__(kFbcThreads) fbc_finish_kernel(const double2* __restrict__ partial, int n,
+                                                                 double* __restrict__ out) {
+  __shared__ double sn[kFbcThreads], sd[kFbcThreads];
+  double a = 0.0, b = 0.0;
+  for (int i = threadIdx.x; i < n; i += kFbcThreads) {
+    a += partial[i].x;
+    b += partial[i].y;
+  }
+  sn[threadIdx.x] = a;
+  sd[threadIdx.x] = b;
+  __syncthreads();
+  for (int o = kFbcThreads / 2; o > 0; o >>= 1) {
+    if (threadIdx.x < o) {
+      sn[threadIdx.x] += sn[threadIdx.x + o];
+      sd[threadIdx.x] += sd[threadIdx.x + o];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    out[0] = sn[0];
+    out[1] = sd[0];
+  }
+}
+
+// Skipped pass: x = x1 + rest per row, with the row's per-256-column sums of squares
+// for the output head's norm. One CTA per row, 16 columns per thread.
+__global__ void __launch_bounds__(256) fbc_apply_kernel(float* __restrict__ x, const float* __restrict__ rest,
+                                                        float* __restrict__ ssp) {
+  const size_t row = blockIdx.x;
+  const int c0 = threadIdx.x * 16;
+  float4* xr = reinterpret_cast<float4*>(x + row * kHidden + c0);
+  const float4* rr = reinterpret_cast<const float4*>(rest + row * kHidden + c0);
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float4 v = xr[i];
+    const float4 r = rr[i];
+    v.x = __fadd_rn(v.x, r.x);
+    v.y = __fadd_rn(v.y, r.y);
+    v.z = __fadd_rn(v.z, r.z);
+    v.w = __fadd_rn(v.w, r.w);
+    xr[i] = v;
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 15) == 0) ssp[row * kSspParts + threadIdx.x / 16] = ss;
+}
+
+// Full pass: rest = x_last - x1 (the residual of blocks 1..last).
+__global__ void fbc_rest_kernel(const float* __restrict__ xl, const float* __restrict__ x1c, float* __restrict__ rest,
+                                long long n4) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const float4 a = reinterpret_cast<const float4*>(xl)[i];
+    const float4 b = reinterpret_cast<const float4*>(x1c)[i];
+    reinterpret_cast<float4*>(rest)[i] =
+        make_float4(__fsub_rn(a.x, b.x), __fsub_rn(a.y, b.y), __fsub_rn(a.z, b.z), __fsub_rn(a.w, b.w));
+  }
+}
+
 // x[t, c] = z[c, t] for t < h*w, c < 64 (32x32 tiles through shared memory).
 __global__ void pack_noise_kernel(const float* __restrict__ z, int T, float* __restrict__ x) {
   __shared__ float tile[32][33];
@@ -442,6 +576,36 @@ cudaError_t launch_euler(float* x, const float* vel, long long n, float s_i, flo
   if (n <= 0) return cudaSuccess;
   const long long threads = (n + 3) / 4;
   euler_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(x, vel, n, s_i, s_next);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dpmpp2m(float* x, const float* vel, float* dprev, long long n, float sigma_i, int order, float a,
+                           float b, float c0, float c1, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const long long threads = (n + 3) / 4;
+  dpmpp2m_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(x, vel, dprev, n, sigma_i, order, a, b,
+                                                                             c0, c1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fbc_residual(const float* x1, const float* x0, const float* ref, float* r0, float* x1c, int rows,
+                                int grid, double2* partial, double* out, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const long long n4 = static_cast<long long>(rows) * kHidden / 4;
+  fbc_residual_kernel<<<grid, kFbcThreads, 0, s>>>(x1, x0, ref, r0, x1c, n4, partial);
+  if (ref) fbc_finish_kernel<<<1, kFbcThreads, 0, s>>>(partial, grid, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fbc_apply(float* x, const float* rest, float* ssp, int rows, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  fbc_apply_kernel<<<rows, 256, 0, s>>>(x, rest, ssp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fbc_rest(const float* xl, const float* x1c, float* rest, int rows, int grid, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  fbc_rest_kernel<<<grid, 256, 0, s>>>(xl, x1c, rest, static_cast<long long>(rows) * kHidden / 4);
   return cudaGetLastError();
 }
 

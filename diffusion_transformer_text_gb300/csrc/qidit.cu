@@ -134,6 +134,17 @@ struct qi_dit {
   float* vel_pos = nullptr;   // [N_max, 64] guidance: conditional velocity (slots == 2)
   float* vel_neg = nullptr;   // [N_max, 64] guidance: negative-prompt velocity
 
+  // first-block cache, image rows only (allocated on first use)
+  float* fbc_x0 = nullptr;            // [N_max, 4096] residual stream entering block 0
+  float* fbc_x1 = nullptr;            // [N_max, 4096] leaving block 0
+  float* fbc_r0[2] = {nullptr, nullptr};  // block 0's residual: reference and this pass
+  float* fbc_rest = nullptr;          // [N_max, 4096] residual of blocks 1..last at the reference
+  double2* fbc_part = nullptr;        // per-CTA sums of the change measure
+  double* fbc_out = nullptr;          // {sum |r0 - ref|, sum |ref|}
+  int fbc_ref = 0;                    // index of the reference in fbc_r0
+  int fbc_N = -1;                     // N of the valid reference, -1 if none
+  int fbc_L = -1;                     // L of the capture the reference was taken with
+
   // host-I/O staging (allocated on first use)
   float *st_img = nullptr, *st_txt = nullptr, *st_tc = nullptr, *st_ts = nullptr, *st_ic = nullptr,
         *st_is = nullptr, *st_vel = nullptr;
@@ -298,31 +309,34 @@ qi_status trace_copy(qi_dit* d, int at_block, int R, cudaStream_t s) {
   return QI_OK;
 }
 
-// The whole pass. Joint: rows [text L | image N]; image: rows [image N] with the
-// stored text K/V; text: rows [text L], no head.
-qi_status run_pass(qi_dit* d, int slot, PassMode mode, const float* img, int N, const float* txt, int L, float t,
-                   const float* tc, const float* ts, const float* ic, const float* is, float* vel,
-                   cudaStream_t s) {
-  d->cur_slot = slot;
-  const int n_text = mode == kImage ? 0 : L;
-  const int n_img = mode == kText ? 0 : N;
-  const int R = n_text + n_img;
-  const int q_off = mode == kImage ? L : 0;
-  const int Lk = mode == kText ? L : L + N;
+// Rows of a pass. Joint: [text L | image N]; image: [image N] with the stored
+// text K/V; text: [text L], no head.
+struct PassRows {
+  int n_text, n_img, R, q_off, Lk;
+  PassRows(PassMode mode, int N, int L)
+      : n_text(mode == kImage ? 0 : L),
+        n_img(mode == kText ? 0 : N),
+        R(n_text + n_img),
+        q_off(mode == kImage ? L : 0),
+        Lk(mode == kText ? L : L + N) {}
+};
 
+// Modulation rows and the input projections: x, xa, ssp for every row of the pass.
+qi_status pass_embed(qi_dit* d, const PassRows& pr, const float* img, int N, const float* txt, int L, float t,
+                     cudaStream_t s) {
   QI_TRY(compute_mod(d, t, s));
   {
     ProfScope ps(d, s, 5);
-    if (n_text > 0) {
+    if (pr.n_text > 0) {
       QI_CUDA(qi::launch_txt_prenorm(txt, L, d->txt_norm_w, d->txt_a, s));
     }
-    if (n_img > 0) {
-      const size_t off = static_cast<size_t>(n_text);
+    if (pr.n_img > 0) {
+      const size_t off = static_cast<size_t>(pr.n_text);
       QI_CUDA(qi::launch_img_in(img, N, d->img_w, d->img_b, d->mod, d->x + off * kHidden, d->xa + off * kHidden,
                                 d->ssp + off * kSspParts, s));
     }
   }
-  if (n_text > 0) {
+  if (pr.n_text > 0) {
     ProfScope ps(d, s, 5);
     CUtensorMap m_a;
     QI_TRY(make_map(&m_a, d->txt_a, L, kHidden, 128));
@@ -342,17 +356,39 @@ qi_status run_pass(qi_dit* d, int slot, PassMode mode, const float* img, int N, 
     g.scale_chunk = 0;
     QI_CUDA(qi::launch_gemm(qi::kEpiResid, m_a, d->m_txt, g, d->num_sms, s));
   }
-  for (int b = 0; b < d->blocks; ++b) {
-    QI_TRY(trace_copy(d, b, R, s));
-    QI_TRY(run_block(d, b, R, n_text, q_off, L, Lk, tc, ts, ic, is, s));
-  }
-  QI_TRY(trace_copy(d, d->blocks, R, s));
-  if (n_img > 0) {
-    ProfScope ps(d, s, 5);
-    const size_t off = static_cast<size_t>(n_text);
-    QI_CUDA(qi::launch_head(d->x + off * kHidden, N, d->ssp + off * kSspParts, d->out_w, d->out_b, vel, d->err, s));
-  }
   return QI_OK;
+}
+
+// Blocks b0 .. b1-1 over the pass's rows.
+qi_status pass_blocks(qi_dit* d, const PassRows& pr, int b0, int b1, int L, const float* tc, const float* ts,
+                      const float* ic, const float* is, cudaStream_t s) {
+  for (int b = b0; b < b1; ++b) {
+    QI_TRY(trace_copy(d, b, pr.R, s));
+    QI_TRY(run_block(d, b, pr.R, pr.n_text, pr.q_off, L, pr.Lk, tc, ts, ic, is, s));
+  }
+  if (b1 == d->blocks) QI_TRY(trace_copy(d, d->blocks, pr.R, s));
+  return QI_OK;
+}
+
+// Output head on the image rows (needs their ssp partials).
+qi_status pass_head(qi_dit* d, const PassRows& pr, int N, float* vel, cudaStream_t s) {
+  if (pr.n_img == 0) return QI_OK;
+  ProfScope ps(d, s, 5);
+  const size_t off = static_cast<size_t>(pr.n_text);
+  QI_CUDA(qi::launch_head(d->x + off * kHidden, N, d->ssp + off * kSspParts, d->out_w, d->out_b, vel, d->err, s));
+  return QI_OK;
+}
+
+qi_status run_pass(qi_dit* d, int slot, PassMode mode, const float* img, int N, const float* txt, int L, float t,
+                   const float* tc, const float* ts, const float* ic, const float* is, float* vel,
+                   cudaStream_t s) {
+  d->cur_slot = slot;
+  // a pass that rewrites slot 0's text K/V starts a new run for the first-block cache
+  if (slot == 0 && mode != kImage) d->fbc_N = -1;
+  const PassRows pr(mode, N, L);
+  QI_TRY(pass_embed(d, pr, img, N, txt, L, t, s));
+  QI_TRY(pass_blocks(d, pr, 0, d->blocks, L, tc, ts, ic, is, s));
+  return pass_head(d, pr, N, vel, s);
 }
 
 // bf16 -> fp16 in place for tensor-core weights; synchronises `s`. A value beyond
@@ -528,9 +564,12 @@ qi_status qi_dit_destroy(qi_dit* d) {
     cudaEventDestroy(e.a);
     cudaEventDestroy(e.b);
   }
-  float* st[] = {d->st_img, d->st_txt, d->st_tc, d->st_ts, d->st_ic, d->st_is, d->st_vel};
+  float* st[] = {d->st_img, d->st_txt, d->st_tc, d->st_ts, d->st_ic, d->st_is, d->st_vel,
+                 d->fbc_x0, d->fbc_x1, d->fbc_r0[0], d->fbc_r0[1], d->fbc_rest};
   for (float* p : st)
     if (p) cudaFree(p);
+  if (d->fbc_part) cudaFree(d->fbc_part);
+  if (d->fbc_out) cudaFree(d->fbc_out);
   cudaFree(d->amem);
   cudaFree(d->wmem);
   delete d;
@@ -654,6 +693,55 @@ qi_status qi_euler_update(float* x, const float* vel, int N, float sigma_i, floa
   return QI_OK;
 }
 
+// DPM++ 2M coefficients of step i, in float64 from the float32 sigmas, rounded once.
+// lambda(sigma) = log(1 - sigma) - log(sigma) is only needed for the ratio of two
+// step sizes; a and b need no logarithm (alpha = 1 - sigma).
+qi_status qi_dpmpp2m_coeffs(const float* sigmas, int steps, int i, int* order, float* coeffs) {
+  if (!sigmas || !order || !coeffs) return fail(QI_ERR_INVALID_ARG, "qi_dpmpp2m_coeffs: NULL argument");
+  if (steps < 1) return fail(QI_ERR_SHAPE, "qi_dpmpp2m_coeffs: steps %d", steps);
+  if (i < 0 || i >= steps) return fail(QI_ERR_INVALID_ARG, "qi_dpmpp2m_coeffs: step %d of %d", i, steps);
+  const double s = sigmas[i], sn = sigmas[i + 1];
+  const double sp = i > 0 ? static_cast<double>(sigmas[i - 1]) : 1.0;
+  if (!(s <= 1.0 && sn >= 0.0 && sn < s && (i == 0 || (sp <= 1.0 && sp > s))))
+    return fail(QI_ERR_INVALID_ARG, "qi_dpmpp2m_coeffs: sigmas around step %d are not decreasing within [0, 1]", i);
+  if (sn == 0.0) {
+    *order = 0;
+    coeffs[0] = 0.f;
+    coeffs[1] = 1.f;
+    coeffs[2] = 1.f;
+    coeffs[3] = 0.f;
+    return QI_OK;
+  }
+  coeffs[0] = static_cast<float>(sn / s);
+  coeffs[1] = static_cast<float>((s - sn) / s);
+  if (i == 0 || sp >= 1.0) {
+    *order = 1;
+    coeffs[2] = 1.f;
+    coeffs[3] = 0.f;
+    return QI_OK;
+  }
+  auto lambda = [](double v) { return std::log1p(-v) - std::log(v); };
+  const double h = lambda(sn) - lambda(s);
+  const double h_prev = lambda(s) - lambda(sp);
+  const double c1 = h / (2.0 * h_prev);
+  *order = 2;
+  coeffs[2] = static_cast<float>(1.0 + c1);
+  coeffs[3] = static_cast<float>(c1);
+  return QI_OK;
+}
+
+qi_status qi_dpmpp2m_update(float* x, const float* vel, float* d_prev, int N, const float* sigmas, int steps, int i,
+                            qi_stream_t stream) {
+  if (!x || !vel || !d_prev) return fail(QI_ERR_INVALID_ARG, "qi_dpmpp2m_update: NULL argument");
+  if (N < 0) return fail(QI_ERR_SHAPE, "qi_dpmpp2m_update: N %d", N);
+  int order = 0;
+  float c[4];
+  QI_TRY(qi_dpmpp2m_coeffs(sigmas, steps, i, &order, c));
+  QI_CUDA(qi::launch_dpmpp2m(x, vel, d_prev, static_cast<long long>(N) * kPatch, sigmas[i], order, c[0], c[1], c[2],
+                             c[3], reinterpret_cast<cudaStream_t>(stream)));
+  return QI_OK;
+}
+
 qi_status qi_dit_step(qi_dit* d, const float* img_tokens, int N, const float* txt_feats, int L, float timestep,
                       const float* txt_cos, const float* txt_sin, const float* img_cos, const float* img_sin,
                       float* vel, unsigned flags, qi_stream_t stream) {
@@ -742,6 +830,87 @@ qi_status qi_dit_step_cfg(qi_dit* d, const float* img_tokens, int N, float times
     d->cache_L[0] = L_pos;
     d->cache_L[1] = L_neg;
   }
+  return QI_OK;
+}
+
+qi_status qi_dit_step_fbcache(qi_dit* d, const float* img_tokens, int N, const float* txt_feats, int L,
+                              float timestep, const float* txt_cos, const float* txt_sin, const float* img_cos,
+                              const float* img_sin, float threshold, float* vel, float* rel_change, int* skipped,
+                              unsigned flags, qi_stream_t stream) {
+  if (!d) return fail(QI_ERR_INVALID_ARG, "qi_dit_step_fbcache: NULL handle");
+  if (flags & ~QI_STEP_USE_CACHE) return fail(QI_ERR_INVALID_ARG, "qi_dit_step_fbcache: flags %u", flags);
+  const bool use_cache = flags & QI_STEP_USE_CACHE;
+  if (N < QI_N_MIN || N > d->N_max || L < QI_L_MIN || L > d->L_max)
+    return fail(QI_ERR_SHAPE, "qi_dit_step_fbcache: N %d (max %d) L %d (max %d)", N, d->N_max, L, d->L_max);
+  if (!img_tokens || !img_cos || !img_sin || !vel)
+    return fail(QI_ERR_INVALID_ARG, "qi_dit_step_fbcache: NULL image tensor");
+  if (!use_cache && (!txt_feats || !txt_cos || !txt_sin))
+    return fail(QI_ERR_INVALID_ARG, "qi_dit_step_fbcache: joint pass needs txt_feats and txt_cos/txt_sin");
+  if (use_cache && d->cache_L[0] != L)
+    return fail(QI_ERR_STATE, "qi_dit_step_fbcache: USE_CACHE but the capture is for L=%d, not %d", d->cache_L[0], L);
+  if (!all_loaded(d)) return fail(QI_ERR_STATE, "qi_dit_step_fbcache: weights not loaded");
+  if (!std::isfinite(timestep) || std::isnan(threshold))
+    return fail(QI_ERR_INVALID_ARG, "qi_dit_step_fbcache: timestep or threshold not a number");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  QI_CUDA(cudaSetDevice(d->device));
+  const size_t img_bytes = static_cast<size_t>(d->N_max) * kHidden * sizeof(float);
+  const int grid = 4 * d->num_sms;
+  if (!d->fbc_x0) {
+    QI_CUDA(cudaMalloc(&d->fbc_x0, img_bytes));
+    QI_CUDA(cudaMalloc(&d->fbc_x1, img_bytes));
+    QI_CUDA(cudaMalloc(&d->fbc_r0[0], img_bytes));
+    QI_CUDA(cudaMalloc(&d->fbc_r0[1], img_bytes));
+    QI_CUDA(cudaMalloc(&d->fbc_rest, img_bytes));
+    QI_CUDA(cudaMalloc(&d->fbc_part, static_cast<size_t>(grid) * sizeof(double2)));
+    QI_CUDA(cudaMalloc(&d->fbc_out, 2 * sizeof(double)));
+  }
+  d->cur_slot = 0;
+  const PassMode mode = use_cache ? kImage : kJoint;
+  const PassRows pr(mode, N, L);
+  const size_t off = static_cast<size_t>(pr.n_text) * kHidden;
+  // a joint pass starts a new run: no reference; so does a different image size or prompt
+  const bool have_ref = use_cache && d->fbc_N == N && d->fbc_L == L;
+
+  QI_TRY(pass_embed(d, pr, img_tokens, N, txt_feats, L, timestep, s));
+  QI_CUDA(cudaMemcpyAsync(d->fbc_x0, d->x + off, static_cast<size_t>(N) * kHidden * sizeof(float),
+                          cudaMemcpyDeviceToDevice, s));
+  QI_TRY(pass_blocks(d, pr, 0, 1, L, txt_cos, txt_sin, img_cos, img_sin, s));
+  float* r0 = d->fbc_r0[d->fbc_ref ^ 1];
+  {
+    ProfScope ps(d, s, 5);
+    QI_CUDA(qi::launch_fbc_residual(d->x + off, d->fbc_x0, have_ref ? d->fbc_r0[d->fbc_ref] : nullptr, r0,
+                                    d->fbc_x1, N, grid, d->fbc_part, d->fbc_out, s));
+  }
+  double rel = INFINITY;
+  if (have_ref) {
+    double h[2] = {0.0, 0.0};
+    QI_CUDA(cudaMemcpyAsync(h, d->fbc_out, sizeof(h), cudaMemcpyDeviceToHost, s));
+    QI_CUDA(cudaStreamSynchronize(s));
+    rel = h[1] > 0.0 ? h[0] / h[1] : (h[0] == 0.0 ? 0.0 : INFINITY);
+  }
+  const bool skip = have_ref && rel < static_cast<double>(threshold);
+  if (skip) {
+    ProfScope ps(d, s, 5);
+    QI_CUDA(qi::launch_fbc_apply(d->x + off, d->fbc_rest, d->ssp + static_cast<size_t>(pr.n_text) * kSspParts, N, s));
+  } else {
+    QI_TRY(pass_blocks(d, pr, 1, d->blocks, L, txt_cos, txt_sin, img_cos, img_sin, s));
+    ProfScope ps(d, s, 5);
+    QI_CUDA(qi::launch_fbc_rest(d->x + off, d->fbc_x1, d->fbc_rest, N, grid, s));
+    d->fbc_ref ^= 1;
+    d->fbc_N = N;
+    d->fbc_L = L;
+  }
+  QI_TRY(pass_head(d, pr, N, vel, s));
+  if (!use_cache) d->cache_L[0] = L;
+  if (rel_change) *rel_change = static_cast<float>(rel);
+  if (skipped) *skipped = skip ? 1 : 0;
+  return QI_OK;
+}
+
+qi_status qi_dit_fbcache_reset(qi_dit* d) {
+  if (!d) return fail(QI_ERR_INVALID_ARG, "qi_dit_fbcache_reset: NULL handle");
+  d->fbc_N = -1;
+  d->fbc_L = -1;
   return QI_OK;
 }
 

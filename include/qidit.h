@@ -197,6 +197,31 @@ qi_status qi_pack_noise(const float* z, int h, int w, float* x, qi_stream_t stre
 qi_status qi_euler_update(float* x, const float* vel, int N, float sigma_i, float sigma_next,
                           qi_stream_t stream);
 
+/* DPM++ 2M sampler [MLX page, "Optional modes (approximate or slower)": offered
+ * next to Euler, no formula given]. Reading: the multistep second-order
+ * DPM-Solver++ (Lu et al. 2022) on the flow-matching schedule alpha = 1 - sigma,
+ * lambda = log(alpha / sigma), with the data prediction D = x - sigma * vel.
+ * Step i (sigma_i -> sigma_{i+1}), a = sigma_{i+1} / sigma_i, b = 1 - a:
+ *   order 2:  x <- a x + b (c0 D - c1 D_prev),  c1 = h_i / (2 h_{i-1}), c0 = 1 + c1,
+ *             h_i = lambda_{i+1} - lambda_i;
+ *   order 1:  x <- a x + b D   (i = 0, or sigma_{i-1} = 1 where lambda = -inf);
+ *   order 0:  x <- D           (sigma_{i+1} = 0, the last step).
+ *
+ * qi_dpmpp2m_coeffs (host only, no device work): the step's order and
+ * coefficients {a, b, c0, c1}, each evaluated in float64 from the float32 sigmas
+ * and rounded once to float32. sigmas: HOST [steps + 1]; coeffs: HOST [4].
+ * Errors: INVALID_ARG (NULL, i outside 0..steps-1, sigmas not decreasing from
+ * <= 1 to >= 0 over steps i-1..i+1), SHAPE (steps < 1).
+ *
+ * qi_dpmpp2m_update: applies step i in float32, every operation rounded on its
+ * own (no FMA): D = x - fl(sigma_i vel); order 2: D' = fl(c0 D) - fl(c1 D_prev);
+ * x = fl(a x) + fl(b D'). Then d_prev <- D for step i + 1. x, vel, d_prev:
+ * device [N, 64] float32; d_prev is read only by second-order steps (its
+ * contents may be anything before step 0). sigmas: HOST [steps + 1]. */
+qi_status qi_dpmpp2m_coeffs(const float* sigmas, int steps, int i, int* order, float* coeffs);
+qi_status qi_dpmpp2m_update(float* x, const float* vel, float* d_prev, int N, const float* sigmas,
+                            int steps, int i, qi_stream_t stream);
+
 /* ------------------------------------------------------------------ DiT */
 
 /* One DiT forward pass [ARCH; HOST s1]: vel [N, 64] from img_tokens [N, 64],
@@ -235,6 +260,36 @@ qi_status qi_dit_step_cfg(qi_dit* dit, const float* img_tokens, int N, float tim
                           const float* pos_img_cos, const float* pos_img_sin, const float* neg_feats, int L_neg,
                           const float* neg_txt_cos, const float* neg_txt_sin, const float* neg_img_cos,
                           const float* neg_img_sin, float* vel, unsigned flags, qi_stream_t stream);
+
+/* First-block cache, "Fast mode" [MLX page, "Optional modes (approximate or
+ * slower)": block 0 always runs; blocks 1 to 31 are skipped while block 0's
+ * residual changes less than a threshold; options table: 0.08]. Approximate.
+ *
+ * One qi_dit_step (same arguments and flags, QI_STEP_HOST_IO excepted) under the
+ * cache. Block 0 runs on every row; r0 = x1 - x0 on the image rows (x0 entering
+ * block 0, x1 leaving it) is compared with the reference r0_ref of the last call
+ * that ran every block: rel = sum |r0 - r0_ref| / sum |r0_ref| (fp32 terms, fp64
+ * sums). If rel < threshold the call skips blocks 1..last and the head reads
+ * x1 + rest, where rest = x_last - x1 of the reference call; otherwise it runs
+ * every block and becomes the new reference (r0_ref, rest). There is no
+ * reference after qi_dit_fbcache_reset, a joint pass (any entry point), a text
+ * capture, or a change of N or L; such a call runs every block (rel = +inf).
+ *
+ * threshold: skip when rel < threshold (0 never skips). rel_change, skipped: HOST
+ * outputs (may be NULL): the measure (+inf without a reference) and 1 if blocks
+ * were skipped. With a reference the call synchronises `stream` to read the
+ * measure. The first call allocates 5 x N_max x 4096 float32 of device memory
+ * for the cache (held until qi_dit_destroy).
+ * Errors: as qi_dit_step; INVALID_ARG for QI_STEP_HOST_IO or a NaN threshold. */
+qi_status qi_dit_step_fbcache(qi_dit* dit, const float* img_tokens, int N, const float* txt_feats,
+                              int L, float timestep, const float* txt_cos, const float* txt_sin,
+                              const float* img_cos, const float* img_sin, float threshold,
+                              float* vel, float* rel_change, int* skipped, unsigned flags,
+                              qi_stream_t stream);
+
+/* Drops the first-block cache's reference: the next qi_dit_step_fbcache runs every
+ * block. Host only. Errors: INVALID_ARG (NULL). */
+qi_status qi_dit_fbcache_reset(qi_dit* dit);
 
 /* Text-only pass [REUSE]: run the L text rows (t = 0 modulation, causal over
  * text) through every block and store their K/V, the same values a joint pass

@@ -104,3 +104,30 @@ def test_kv_slots_range(qi):
     assert L.qi_dit_create(ctypes.byref(qi.DitConfig(1, 8, 64, -1)), 0, ctypes.byref(h)) == 2
     assert L.qi_dit_step_cfg(None, None, 64, 0.5, 2.0, None, 8, None, None, None, None, None, 8, None, None,
                              None, None, None, 0, None) == 1
+
+
+@pytest.mark.parametrize("N", [256, 1024, 4096, 16384])
+@pytest.mark.parametrize("steps", [2, 3, 20, 40])
+def test_dpmpp2m_coeffs_bit_exact(qi, N, steps):
+    s, _ = sched.flow_sigmas(steps, N)
+    for i in range(steps):
+        got = qi.dpmpp2m_coeffs(s, i)
+        ref = sched.dpmpp2m_coeffs(s, i)
+        assert got[0] == ref[0], (i, got, ref)
+        assert np.array(got[1:], np.float32).tobytes() == np.array(ref[1:], np.float32).tobytes(), (i, got, ref)
+
+
+def test_dpmpp2m_coeffs_custom_schedule_and_errors(qi):
+    s = np.array([0.9, 0.6, 0.35, 0.1, 0.0], np.float32)
+    for i in range(4):
+        got, ref = qi.dpmpp2m_coeffs(s, i), sched.dpmpp2m_coeffs(s, i)
+        assert got[0] == ref[0] and np.array(got[1:], np.float32).tobytes() == np.array(ref[1:], np.float32).tobytes()
+    with pytest.raises(qi.QiError) as e:
+        qi.dpmpp2m_coeffs(s, 4)                    # step index past the end
+    assert e.value.status == 1
+    with pytest.raises(qi.QiError) as e:
+        qi.dpmpp2m_coeffs(np.array([0.5, 0.7, 0.0], np.float32), 0)   # increasing
+    assert e.value.status == 1
+    with pytest.raises(qi.QiError) as e:
+        qi.dpmpp2m_coeffs(np.array([1.5, 0.7, 0.0], np.float32), 1)   # sigma above 1
+    assert e.value.status == 1

@@ -131,6 +131,26 @@ def test_euler_bit_exact(qi, N):
     assert xt.cpu().numpy().tobytes() == osched.euler_update(x, v, s[7], s[8]).tobytes()
 
 
+@pytest.mark.parametrize("N", [64, 4096, 16384])
+def test_dpmpp2m_loop_bit_exact(qi, N):
+    """A whole 40-step DPM++ 2M loop (orders 1, 1, 2 ... 2, 0) over a velocity that
+    changes every step, against the oracle; every step's x and carried D bit for bit."""
+    import torch
+    s, _ = osched.flow_sigmas(40, N)
+    x = synth.input_f32(6, 52, (N, 64))
+    xt = f32_tensor(x)
+    dt = torch.full((N, 64), float("nan"), device="cuda")   # contents before step 0 are never read
+    dp = None
+    for i in range(40):
+        v = (synth.input_f32(6, 100 + i, (N, 64)) + 0.5 * x).astype(np.float32)
+        x, dp = osched.dpmpp2m_update(x, v, dp, s, i)
+        qi.dpmpp2m_update(xt, f32_tensor(v), dt, s, i)
+        if i in (0, 1, 2, 20, 39):
+            assert xt.cpu().numpy().tobytes() == x.tobytes(), i
+            assert dt.cpu().numpy().tobytes() == dp.tobytes(), i
+    assert xt.cpu().numpy().tobytes() == x.tobytes()
+
+
 @pytest.mark.parametrize("h,w", [(8, 8), (64, 64), (5, 3)])
 def test_pack_noise_exact(qi, h, w):
     z = synth.input_f32(4, 2, (64, h, w))
