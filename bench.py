@@ -311,6 +311,55 @@ def run_ours(args, rank, world, local_rank):
     dit.check()
     cfg_ms = c0.elapsed_time(c1) / CFG_STEPS
 
+    # ---- DPM++ 2M sampler: the same DiT passes with the second-order multistep update
+    DPM_STEPS = 10
+    d_prev = torch.empty_like(x)
+    x.copy_(x0)
+    torch.cuda.synchronize()
+    p0 = torch.cuda.Event(enable_timing=True)
+    p1 = torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for i in range(DPM_STEPS):
+        if i == 0:
+            dit.step(x, txt, tvals[0], tc, tsn, ic, isn, vel=vel)
+        else:
+            dit.step_cached(x, L, tvals[i], ic, isn, vel=vel)
+        qi.dpmpp2m_update(x, vel, d_prev, sig, i)
+    p1.record(stream)
+    torch.cuda.synchronize()
+    dit.check()
+    dpm_ms = p0.elapsed_time(p1) / DPM_STEPS
+
+    # ---- first-block cache ("Fast mode") at the pages' threshold 0.08, Euler loop
+    FB_STEPS, FB_THR = 10, 0.08
+    x.copy_(x0)
+    torch.cuda.synchronize()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    skips, rels = 0, []
+    f0.record(stream)
+    for i in range(FB_STEPS):
+        _, rel, sk = dit.step_fbcache(x, txt, L, tvals[i], tc, tsn, ic, isn, FB_THR, use_cache=i > 0, vel=vel)
+        skips += sk
+        rels.append(rel)
+        qi.euler_update(x, vel, float(sig[i]), float(sig[i + 1]))
+    f1.record(stream)
+    torch.cuda.synchronize()
+    fb_ms = f0.elapsed_time(f1) / FB_STEPS
+    # a call that skips blocks 1..31: the same input again has zero change
+    SKIP_REPS = 5
+    dit.step_fbcache(x, txt, L, tvals[FB_STEPS], tc, tsn, ic, isn, FB_THR, use_cache=True, vel=vel)
+    torch.cuda.synchronize()
+    f0.record(stream)
+    skipped_all = True
+    for i in range(SKIP_REPS):
+        _, rel, sk = dit.step_fbcache(x, txt, L, tvals[FB_STEPS], tc, tsn, ic, isn, FB_THR, use_cache=True, vel=vel)
+        skipped_all &= sk
+    f1.record(stream)
+    torch.cuda.synchronize()
+    dit.check()
+    skip_ms = f0.elapsed_time(f1) / SKIP_REPS
+
     # ---- end to end through the public API with host buffers
     xh = torch.empty(N, 64, dtype=torch.float32).pin_memory()
     xh.copy_(x0.cpu())
@@ -387,6 +436,14 @@ def run_ours(args, rank, world, local_rank):
         "cfg": {"steps_per_s": world * 1e3 / cfg_ms, "ms_per_step": cfg_ms, "guidance": GUIDE, "neg_tokens": L_NEG,
                 "steps": CFG_STEPS, "note": "two passes per step (conditional + negative prompt), 1 joint + "
                                             f"{CFG_STEPS - 1} image-only"},
+        "dpmpp2m": {"steps_per_s": world * 1e3 / dpm_ms, "ms_per_step": dpm_ms, "steps": DPM_STEPS,
+                    "note": "DPM++ 2M update in place of Euler, 1 joint + image-only passes"},
+        "fbcache": {"threshold": FB_THR, "steps": FB_STEPS, "skipped": skips, "ms_per_step": fb_ms,
+                    "steps_per_s": world * 1e3 / fb_ms, "rel_change": [None if r == float("inf") else r for r in rels],
+                    "skipped_call_ms": skip_ms if skipped_all else None,
+                    "note": "Euler loop under the first-block cache; random-init weights change block 0's "
+                            "residual by ~0.9 per step, so nothing is skipped there; skipped_call_ms times a "
+                            "call that skips blocks 1..31 (same input again)"},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         times = oracle_block_sample(9)
