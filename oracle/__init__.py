@@ -13,6 +13,7 @@ sched      FlowMatch Euler sigmas, timesteps, Euler update (host contract s6),
 attention  block-causal attention: masked dense, two-segment, brute force
 dit        timestep embedding, shared modulation, block, full DiT, output head
 fbcache    first-block cache ("Fast mode") around the DiT pass (MLX page)
+mx         MXFP8 block-scaled operands and the block with MXFP8 GEMMs
 
 Everything is numpy float32 (bf16 weights widened exactly); the brute-force
 checkers use Python float64 loops on tiny shapes.
