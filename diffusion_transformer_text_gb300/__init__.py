@@ -40,6 +40,7 @@ SYMBOLS = (
     "qi_dit_block_forward", "qi_dit_read_kv", "qi_dit_set_trace", "qi_dit_profile",
     "qi_dit_profile_read", "qi_last_error", "qi_gemm_bf16", "qi_attention_f16", "qi_gemm_bf16_noalloc",
     "qi_dit_step_cfg", "qi_dpmpp2m_coeffs", "qi_dpmpp2m_update", "qi_dit_step_fbcache", "qi_dit_fbcache_reset",
+    "qi_dit_set_mxfp8", "qi_quant_mxfp8", "qi_gemm_mxfp8",
 )
 
 
@@ -50,7 +51,8 @@ class QiError(RuntimeError):
 
 
 class DitConfig(ctypes.Structure):
-    _fields_ = [("blocks", ctypes.c_int), ("L_max", ctypes.c_int), ("N_max", ctypes.c_int), ("kv_slots", ctypes.c_int)]
+    _fields_ = [("blocks", ctypes.c_int), ("L_max", ctypes.c_int), ("N_max", ctypes.c_int), ("kv_slots", ctypes.c_int),
+                ("mxfp8", ctypes.c_int)]
 
 
 _GLOBAL_FIELDS = ("t_w1", "t_b1", "t_w2", "t_b2", "mod_w", "mod_b", "txt_norm_w", "txt_w", "txt_b",
@@ -109,6 +111,9 @@ def lib() -> ctypes.CDLL:
         "qi_dpmpp2m_coeffs": [P, I, I, P, P],
         "qi_dit_step_fbcache": [P, P, I, P, I, F, P, P, P, P, F, P, P, P, U, P],
         "qi_dit_fbcache_reset": [P],
+        "qi_dit_set_mxfp8": [P, I],
+        "qi_quant_mxfp8": [P, I, I, I, P, P, P],
+        "qi_gemm_mxfp8": [P, P, P, P, P, P, I, I, I, P],
         "qi_dpmpp2m_update": [P, P, P, I, P, I, I, P],
     }
     for name, args in sig.items():
@@ -233,6 +238,17 @@ def dpmpp2m_update(x, vel, d_prev, sigmas, i: int):
     return x
 
 
+def quant_mxfp8(x, bf16: bool):
+    """MXFP8 along the last axis of a [rows, K] 16-bit device tensor (bf16 bits or fp16):
+    returns (E4M3 bytes [rows, K] uint8, scale chunks uint8)."""
+    import torch
+    rows, K = x.shape
+    q = torch.empty(rows, K, dtype=torch.uint8, device=x.device)
+    sf = torch.zeros(((rows + 127) // 128) * (K // 128) * 512, dtype=torch.uint8, device=x.device)
+    _check(lib().qi_quant_mxfp8(_ptr(x), int(bf16), rows, K, _ptr(q), _ptr(sf), _stream()))
+    return q, sf
+
+
 def attention(q, k, v, L: int, q_off: int = 0, Lk: int | None = None):
     """Test hook: block-causal attention, fp16 q [Rq, 4096], k/v [Lk, 4096] -> o [Rq, 4096]."""
     import torch
@@ -249,10 +265,12 @@ def attention(q, k, v, L: int, q_off: int = 0, Lk: int | None = None):
 class DiT:
     """A qi_dit handle: bf16 weight store, activations and per-block text K/V."""
 
-    def __init__(self, blocks: int = 32, L_max: int = 512, N_max: int = 4096, device: int = 0, kv_slots: int = 1):
+    def __init__(self, blocks: int = 32, L_max: int = 512, N_max: int = 4096, device: int = 0, kv_slots: int = 1,
+                 mxfp8: bool = False):
         self.blocks, self.L_max, self.N_max, self.device = blocks, L_max, N_max, device
         h = ctypes.c_void_p()
-        _check(lib().qi_dit_create(ctypes.byref(DitConfig(blocks, L_max, N_max, kv_slots)), device, ctypes.byref(h)))
+        cfg = DitConfig(blocks, L_max, N_max, kv_slots, int(mxfp8))
+        _check(lib().qi_dit_create(ctypes.byref(cfg), device, ctypes.byref(h)))
         self._h = h
 
     def close(self):
@@ -418,6 +436,17 @@ class DiT:
         D = torch.empty(M, N, dtype=torch.float32, device=A.device)
         _check(lib().qi_gemm_bf16(self._h, _ptr(A), _ptr(B), _ptr(D), M, N, K, _stream()))
         return D
+
+    def gemm_mxfp8(self, A, A_sf, B, B_sf, M: int, N: int, K: int):
+        """Test hook: the block-scaled GEMM on operands from quant_mxfp8; D [M, N] float32."""
+        import torch
+        D = torch.empty(M, N, dtype=torch.float32, device=A.device)
+        _check(lib().qi_gemm_mxfp8(self._h, _ptr(A), _ptr(A_sf), _ptr(B), _ptr(B_sf), _ptr(D), M, N, K, _stream()))
+        return D
+
+    def set_mxfp8(self, on: bool):
+        """Run later passes on MXFP8 block GEMMs (handle created with mxfp8=True)."""
+        _check(lib().qi_dit_set_mxfp8(self._h, int(on)))
 
     def set_trace(self, slot: int, block: int, dst=None):
         _check(lib().qi_dit_set_trace(self._h, slot, block, _ptr(dst)))

@@ -6,6 +6,14 @@
 // from the bf16 checkpoint values; [out, in] row-major), fp32 accumulation in
 // tensor memory. The plain fp32 epilogue (a test hook) takes bf16 operands.
 //
+// MXFP8 variant (MX = true): A and B are E4M3 bytes with one UE8M0 scale per 32
+// values along K, stored in 512-byte chunks (128 rows x 4 scales, byte
+// (r % 32) * 16 + ((r % 128) / 32) * 4 + k) ordered [K / 128][rows / 128]. A
+// stage then covers K = 128; its scale chunks arrive by bulk copy with the
+// tiles, are copied into a per-stage set of TMEM columns (tcgen05.cp) and feed
+// four block-scaled MMAs (K = 32 each, the scale byte chosen per MMA). The scale
+// columns leave room for one 256-column accumulator only.
+//
 // Roles per CTA (192 threads):
 //   warp 0     TMA producer: 128x64 A and 256x64 B tiles into a 4-stage ring
 //   warp 1     TMEM owner and MMA issuer (one thread): 4 x tcgen05.mma 128x256x16
@@ -26,9 +34,20 @@ namespace {
 constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;  // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kEpiScratch = 4 * 32 * 33 * 4;  // per epilogue warp: one 32 x 32 fp32 chunk, stride 33
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256 + kEpiScratch;
+constexpr int kSfChunk = 512;                  // MXFP8 scales of 128 rows x 128 K
+
+// Per-variant geometry: the tile bytes are the same (128-byte rows), MXFP8 packs
+// twice the K per stage and adds the scale chunks of A (one) and B (two).
+template <bool MX>
+struct Geo {
+  static constexpr int kSF = MX ? 3 * kSfChunk : 0;
+  static constexpr int kStage = kABytes + kBBytes + kSF;
+  static constexpr int kK = MX ? 128 : kBK;  // K elements per stage
+  static constexpr int kAcc = MX ? 1 : 2;    // TMEM accumulators
+  static constexpr int kSmem = kStages * kStage + 1024 + 256 + kEpiScratch;
+};
+constexpr uint32_t kSfCol = 256;  // MXFP8: stage s scales at columns 256 + 16 s (A: +0..3, B: +4..11)
 // fp16 operands for the DiT epilogues, bf16 for the plain fp32 test hook
 template <int KIND>
 constexpr uint32_t kIdesc = KIND == kEpiF32 ? idesc_bf16_f32(kBM, kBN) : idesc_f16_f32(kBM, kBN);
@@ -226,15 +245,17 @@ __device__ __forceinline__ void epi_f32(const GemmParams& p, uint32_t taddr, int
 
 // ---------------------------------------------------------------- kernel
 
-template <int KIND>
+template <int KIND, bool MX>
 __global__ void __launch_bounds__(192, 1)
     gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmParams p) {
+  using G = Geo<MX>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint8_t* sSF = sB + kStages * kBBytes;  // MXFP8 scale chunks, G::kSF bytes per stage
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * G::kStage);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
@@ -247,7 +268,7 @@ __global__ void __launch_bounds__(192, 1)
   const int num_m = (p.M + kBM - 1) / kBM;
   const int num_n = p.N / kBN;
   const int total = num_m * num_n;
-  const int kblocks = p.K / kBK;
+  const int kblocks = p.K / G::kK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -292,9 +313,15 @@ __global__ void __launch_bounds__(192, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
-          tma_load_2d(sA + stage * kABytes, &tmA, &full[stage], kb * kBK, mt * kBM);
-          tma_load_2d(sB + stage * kBBytes, &tmB, &full[stage], kb * kBK, nt * kBN);
+          mbar_arrive_expect_tx(&full[stage], G::kStage);
+          tma_load_2d(sA + stage * kABytes, &tmA, &full[stage], kb * G::kK, mt * kBM);
+          tma_load_2d(sB + stage * kBBytes, &tmB, &full[stage], kb * G::kK, nt * kBN);
+          if (MX) {
+            uint8_t* sf = sSF + stage * G::kSF;
+            bulk_load(sf, p.sfa + (static_cast<size_t>(kb) * num_m + mt) * kSfChunk, kSfChunk, &full[stage]);
+            bulk_load(sf + kSfChunk, p.sfb + (static_cast<size_t>(kb) * (p.N / 128) + 2 * nt) * kSfChunk,
+                      2 * kSfChunk, &full[stage]);
+          }
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -332,10 +359,24 @@ __global__ void __launch_bounds__(192, 1)
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + stage * kABytes);
           const uint32_t b0 = smem_u32(sB + stage * kBBytes);
+          if (MX) {
+            // this stage's scale set: the MMAs that last read it (kStages stages ago)
+            // completed before the producer could refill the stage
+            const uint32_t sf_t = tmem_base + kSfCol + 16 * stage;
+            const uint32_t sf_s = smem_u32(sSF + stage * G::kSF);
+            tmem_cp_sf(sf_t, plain_rows16_desc(sf_s));
+            tmem_cp_sf(sf_t + 4, plain_rows16_desc(sf_s + kSfChunk));
+            tmem_cp_sf(sf_t + 8, plain_rows16_desc(sf_s + 2 * kSfChunk));
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            mma_ss(d, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k), kIdesc<KIND>,
-                        (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < 4; ++k)
+              mma_mxf8(d, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k),
+                       idesc_mxf8_f32(kBM, kBN, static_cast<uint32_t>(k)), sf_t, sf_t + 4, (kb | k) != 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              mma_ss(d, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k), kIdesc<KIND>,
+                     (kb | k) != 0 ? 1u : 0u);
+          }
           mma_commit(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;
@@ -344,8 +385,10 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (!ok) break;
         mma_commit(&tfull[acc]);
-        acc ^= 1u;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == G::kAcc) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
       // all MMAs of this thread must finish before TMEM is released
       mma_commit(drain);
@@ -373,7 +416,7 @@ __global__ void __launch_bounds__(192, 1)
         epi_qkv(p, taddr, row, nt * kBN);
       else if (KIND == kEpiResid)
         epi_resid(p, taddr, mt * kBM + quarter * 32, lane, nt * kBN,
-                  reinterpret_cast<float*>(smem + kStages * kStageBytes + 256) + (warp - 2) * 32 * 33);
+                  reinterpret_cast<float*>(smem + kStages * G::kStage + 256) + (warp - 2) * 32 * 33);
       else if (KIND == kEpiSwiglu)
         epi_swiglu(p, taddr, row, nt * kBN);
       else
@@ -381,8 +424,10 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
-      acc ^= 1u;
-      if (acc == 0) acc_phase ^= 1u;
+      if (++acc == G::kAcc) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
     }
   }
 
@@ -393,38 +438,51 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-template <int KIND>
+template <int KIND, bool MX>
 cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
                         cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_bf16_tc<KIND, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<MX>::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_bf16_tc<KIND><<<grid, 192, kSmemBytes, stream>>>(a, b, p);
+  gemm_bf16_tc<KIND, MX><<<grid, 192, Geo<MX>::kSmem, stream>>>(a, b, p);
   return cudaGetLastError();
+}
+
+template <bool MX>
+cudaError_t launch_any(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                       int grid_ctas, cudaStream_t stream) {
+  if (p.M <= 0) return cudaSuccess;
+  if (p.N % kBN != 0 || p.K % Geo<MX>::kK != 0) return cudaErrorInvalidValue;
+  if (MX && (p.sfa == nullptr || p.sfb == nullptr)) return cudaErrorInvalidValue;
+  const int tiles = ((p.M + kBM - 1) / kBM) * (p.N / kBN);
+  const int grid = tiles < grid_ctas ? tiles : grid_ctas;
+  switch (kind) {
+    case kEpiQkv:
+      return launch_kind<kEpiQkv, MX>(a, b, p, grid, stream);
+    case kEpiResid:
+      return launch_kind<kEpiResid, MX>(a, b, p, grid, stream);
+    case kEpiSwiglu:
+      return launch_kind<kEpiSwiglu, MX>(a, b, p, grid, stream);
+    case kEpiF32:
+      return launch_kind<kEpiF32, MX>(a, b, p, grid, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                         int grid_ctas, cudaStream_t stream) {
-  if (p.M <= 0) return cudaSuccess;
-  if (p.N % kBN != 0 || p.K % kBK != 0) return cudaErrorInvalidValue;
-  const int tiles = ((p.M + kBM - 1) / kBM) * (p.N / kBN);
-  const int grid = tiles < grid_ctas ? tiles : grid_ctas;
-  switch (kind) {
-    case kEpiQkv:
-      return launch_kind<kEpiQkv>(a, b, p, grid, stream);
-    case kEpiResid:
-      return launch_kind<kEpiResid>(a, b, p, grid, stream);
-    case kEpiSwiglu:
-      return launch_kind<kEpiSwiglu>(a, b, p, grid, stream);
-    case kEpiF32:
-      return launch_kind<kEpiF32>(a, b, p, grid, stream);
-  }
-  return cudaErrorInvalidValue;
+  return launch_any<false>(kind, a, b, p, grid_ctas, stream);
+}
+
+cudaError_t launch_gemm_mx(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                           int grid_ctas, cudaStream_t stream) {
+  return launch_any<true>(kind, a, b, p, grid_ctas, stream);
 }
 
 }  // namespace qi

@@ -76,6 +76,9 @@ struct GemmParams {
   int scale_chunk;          // modulation chunk used as (1 + scale) for xa
   float* d;                 // kEpiF32: D [M][N]
   int* err;                 // device error word
+  // MXFP8 variant: scale chunks of A (ceil(M/128) row groups) and B (N/128 groups)
+  const uint8_t* sfa;
+  const uint8_t* sfb;
 };
 
 // Launch one persistent tcgen05 GEMM D[M,N] = A[M,K] * B[N,K]^T with the
@@ -83,6 +86,22 @@ struct GemmParams {
 // {64, 256}; the operands are fp16 for the DiT epilogues and bf16 for kEpiF32.
 cudaError_t launch_gemm(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                         int grid_ctas, cudaStream_t stream);
+
+// The MXFP8 variant: A and B maps are 2-D 8-bit maps with box {128, 128} /
+// {128, 256}; p.sfa / p.sfb hold the UE8M0 scale chunks (layout in gemm.cu,
+// written by launch_quant_mx). K must be a multiple of 128.
+cudaError_t launch_gemm_mx(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                           int grid_ctas, cudaStream_t stream);
+
+// 2-D 8-bit map over a row-major [rows, cols] byte matrix, box = box_rows x 128
+// columns with 128-byte swizzle (qidit.cu).
+bool encode_map8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+
+// MXFP8 quantisation of a row-major [rows, K] 16-bit matrix (bf16 bits if `bf16`,
+// else fp16) along K: q [rows, K] E4M3 bytes and the scale chunks for
+// ceil(rows / 128) row groups (kernels_small.cu).
+cudaError_t launch_quant_mx(const uint16_t* in, bool bf16, int rows, int K, uint8_t* q, uint8_t* sf,
+                            cudaStream_t s);
 
 struct AttnParams {
   const act_t* q;  // [Rq][kHidden], query row r has global index r + q_off

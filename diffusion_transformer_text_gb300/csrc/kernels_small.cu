@@ -3,6 +3,8 @@
 // output head, RoPE tables, noise packing and the Euler update.
 #include <math.h>
 
+#include <cuda_fp8.h>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -381,6 +383,63 @@ __global__ void dpmpp2m_kernel(float* __restrict__ x, const float* __restrict__ 
   }
 }
 
+// ---------------------------------------------------------------- MXFP8 quantisation
+
+// One thread per block of 32 values along K: the shared exponent
+// e = floor(log2 max|v|) - 8 (8 = exponent of E4M3's largest normal, 448),
+// clamped to [-127, 127], -127 for an all-zero block; each value becomes
+// E4M3(v * 2^-e), rounded to nearest even and clamped to +-448. Scale byte e + 127
+// goes to chunk (K-group k / 128, row group r / 128), byte
+// (r % 32) * 16 + ((r % 128) / 32) * 4 + (k / 32) % 4.
+template <bool BF16>
+__global__ void quant_mx_kernel(const uint16_t* __restrict__ in, int rows, int K, int groups,
+                                uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  const int per_row = K / 32;
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<long long>(rows) * per_row) return;
+  const int r = static_cast<int>(idx / per_row);
+  const int kb = static_cast<int>(idx - static_cast<long long>(r) * per_row);
+  const uint4* src = reinterpret_cast<const uint4*>(in + static_cast<size_t>(r) * K + kb * 32);
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 w = src[i];
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (BF16) {
+        v[8 * i + 2 * j] = __uint_as_float(u[j] << 16);
+        v[8 * i + 2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+      } else {
+        const __half2 h = *reinterpret_cast<const __half2*>(&u[j]);
+        const float2 f = __half22float2(h);
+        v[8 * i + 2 * j] = f.x;
+        v[8 * i + 2 * j + 1] = f.y;
+      }
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  int e = amax > 0.f ? ilogbf(amax) - 8 : -127;
+  e = max(-127, min(127, e));
+  const float inv = ldexpf(1.f, -e);  // exact power of two
+  uint32_t packed[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i] * inv, v[4 * i + 1] * inv), __NV_SATFINITE,
+                                                 __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i + 2] * inv, v[4 * i + 3] * inv), __NV_SATFINITE,
+                                                 __NV_E4M3);
+    packed[i] = (lo & 0xFFFFu) | (hi << 16);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(q + static_cast<size_t>(r) * K + kb * 32);
+  dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  const size_t chunk = static_cast<size_t>(kb / 4) * groups + r / 128;
+  sf[chunk * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + (kb % 4)] = static_cast<uint8_t>(e + 127);
+}
+
 // ---------------------------------------------------------------- first-block cache
 
 // r0 = x1 - x0 (block 0's residual), copies x1, and (when ref != nullptr) per-CTA sums
@@ -585,6 +644,20 @@ cudaError_t launch_dpmpp2m(float* x, const float* vel, float* dprev, long long n
   const long long threads = (n + 3) / 4;
   dpmpp2m_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(x, vel, dprev, n, sigma_i, order, a, b,
                                                                              c0, c1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_mx(const uint16_t* in, bool bf16, int rows, int K, uint8_t* q, uint8_t* sf,
+                            cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (K % 128 != 0) return cudaErrorInvalidValue;
+  const long long n = static_cast<long long>(rows) * (K / 32);
+  const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
+  const int groups = (rows + 127) / 128;
+  if (bf16)
+    quant_mx_kernel<true><<<blocks, 256, 0, s>>>(in, rows, K, groups, q, sf);
+  else
+    quant_mx_kernel<false><<<blocks, 256, 0, s>>>(in, rows, K, groups, q, sf);
   return cudaGetLastError();
 }
 

@@ -104,6 +104,15 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// Untiled bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16);
+// completion counted as bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 
 // Allocate `ncols` TMEM columns (power of two >= 32); whole warp; address -> *slot.
@@ -260,6 +269,47 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) {
 }
 
 __host__ __device__ constexpr uint32_t idesc_f16_f32_bmn(int M, int N) { return idesc_f16_f32(M, N) | (1u << 16); }
+
+// ------------------------------------------------------------------ block-scaled (MXFP8)
+
+// kind::mxf8f6f4 instruction descriptor: E4M3 A and B (format 0), K-major, fp32
+// accumulator, UE8M0 scale factors (bit 23), N >> 3 at bit 17, M >> 4 at bit 24,
+// and the byte of the 32-bit scale-factor column that this MMA's K=32 slice uses:
+// B's at bits 4-5, A's at bits 29-30.
+__host__ __device__ constexpr uint32_t idesc_mxf8_f32(int M, int N, uint32_t sf_id) {
+  return (sf_id << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) |
+         (sf_id << 29);
+}
+
+// D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T over K = 32, A and B E4M3 in shared memory,
+// per-row / per-column UE8M0 scales in tensor memory. Issued by one thread.
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Shared -> tensor memory copy of one 512-byte scale-factor chunk (32 rows of 16
+// bytes), replicated into all four 32-lane quarters: 4 columns from taddr.
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Descriptor of a contiguous no-swizzle operand of 16-byte rows: 8-row core
+// matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t plain_rows16_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>(128 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
 
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

@@ -112,6 +112,20 @@ struct qi_dit {
   std::vector<Block> blk;
   CUtensorMap m_txt;
 
+  // MXFP8 copies of the block weights (qi_dit_config.mxfp8): E4M3 bytes in the
+  // layouts above plus their scale chunks, and the quantised A operand buffer
+  bool has_mx = false;
+  bool mx_on = false;  // the passes run the MXFP8 GEMMs (qi_dit_set_mxfp8)
+  struct BlockMx {
+    uint8_t *wqkv, *wo, *wgu, *wd;  // E4M3
+    uint8_t *sqkv, *so, *sgu, *sd;  // scale chunks
+    CUtensorMap m_qkv, m_o, m_gu, m_d;
+  };
+  std::vector<BlockMx> bmx;
+  void* mxmem = nullptr;
+  uint8_t* aq = nullptr;   // [R_max, 12288] E4M3 activations (the GEMM's A operand)
+  uint8_t* asf = nullptr;  // their scale chunks
+
   // activations (one allocation)
   void* amem = nullptr;
   float* x = nullptr;      // [R_max, 4096] fp32 residual stream
@@ -214,9 +228,28 @@ qi_status compute_mod(qi_dit* d, float t, cudaStream_t s) {
 
 // One block over `R` activation rows. n_text = rows that are text (they come
 // first); q_off = global index of activation row 0; Lk = keys image rows see.
+// One GEMM of the block: fp16 operands, or (MXFP8 mode) the A operand `a16`
+// quantised into the handle's E4M3 buffer first and the block's MXFP8 weights.
+qi_status block_gemm(qi_dit* d, qi::EpiKind kind, const act_t* a16, int R, int K, const CUtensorMap& m_a16,
+                     const CUtensorMap& m_w16, const CUtensorMap& m_w8, const uint8_t* w_sf, qi::GemmParams g,
+                     cudaStream_t s) {
+  if (!d->mx_on) {
+    QI_CUDA(qi::launch_gemm(kind, m_a16, m_w16, g, d->num_sms, s));
+    return QI_OK;
+  }
+  QI_CUDA(qi::launch_quant_mx(reinterpret_cast<const uint16_t*>(a16), false, R, K, d->aq, d->asf, s));
+  CUtensorMap m_a8;
+  if (!qi::encode_map8(&m_a8, d->aq, R, K, 128)) return fail(QI_ERR_CUDA, "8-bit tensor map encoding failed");
+  g.sfa = d->asf;
+  g.sfb = w_sf;
+  QI_CUDA(qi::launch_gemm_mx(kind, m_a8, m_w8, g, d->num_sms, s));
+  return QI_OK;
+}
+
 qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int Lk, const float* txt_cos,
                     const float* txt_sin, const float* img_cos, const float* img_sin, cudaStream_t s) {
   qi_dit::Block& B = d->blk[b];
+  qi_dit::BlockMx* BM = d->mx_on ? &d->bmx[b] : nullptr;
   CUtensorMap m_xa, m_o, m_h;
   QI_TRY(make_map(&m_xa, d->xa, R, kHidden, 128));
   QI_TRY(make_map(&m_o, d->o, R, kHidden, 128));
@@ -243,7 +276,8 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
     g.txt_sin = txt_sin;
     g.img_cos = img_cos;
     g.img_sin = img_sin;
-    QI_CUDA(qi::launch_gemm(qi::kEpiQkv, m_xa, B.m_qkv, g, d->num_sms, s));
+    QI_TRY(block_gemm(d, qi::kEpiQkv, d->xa, R, kHidden, m_xa, B.m_qkv, BM ? BM->m_qkv : B.m_qkv,
+                      BM ? BM->sqkv : nullptr, g, s));
   }
   // block-causal attention
   {
@@ -272,7 +306,8 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
     g.resid_set = 0;
     g.gate_chunk = 1;
     g.scale_chunk = 2;
-    QI_CUDA(qi::launch_gemm(qi::kEpiResid, m_o, B.m_o, g, d->num_sms, s));
+    QI_TRY(block_gemm(d, qi::kEpiResid, d->o, R, kHidden, m_o, B.m_o, BM ? BM->m_o : B.m_o, BM ? BM->so : nullptr, g,
+                      s));
   }
   // gate/up + SwiGLU
   {
@@ -282,7 +317,8 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
     g.K = kHidden;
     g.ssp_in = d->ssp;
     g.h = d->h;
-    QI_CUDA(qi::launch_gemm(qi::kEpiSwiglu, m_xa, B.m_gu, g, d->num_sms, s));
+    QI_TRY(block_gemm(d, qi::kEpiSwiglu, d->xa, R, kHidden, m_xa, B.m_gu, BM ? BM->m_gu : B.m_gu,
+                      BM ? BM->sgu : nullptr, g, s));
   }
   // down: x += g2 * (h Wd^T); xa = fp16(x (1 + s1)) for the next block
   {
@@ -296,7 +332,8 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
     g.resid_set = 0;
     g.gate_chunk = 3;
     g.scale_chunk = 0;
-    QI_CUDA(qi::launch_gemm(qi::kEpiResid, m_h, B.m_d, g, d->num_sms, s));
+    QI_TRY(block_gemm(d, qi::kEpiResid, d->h, R, kFfn, m_h, B.m_d, BM ? BM->m_d : B.m_d, BM ? BM->sd : nullptr, g,
+                      s));
   }
   return QI_OK;
 }
@@ -428,6 +465,18 @@ bool qi::encode_map16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool qi::encode_map8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || (reinterpret_cast<uintptr_t>(base) & 15) != 0 || cols % 16 != 0 || rows == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ================================================================ C ABI
 
 extern "C" {
@@ -530,6 +579,44 @@ qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out) {
   }
   cudaMemset(d->amem, 0, abytes);
 
+  // ---- MXFP8 weight copies and the quantised activation buffer
+  if (cfg->mxfp8) {
+    const size_t sq = (size_t)kHidden * kHidden;
+    auto sf_bytes = [](size_t rows, size_t K) { return (rows + 127) / 128 * (K / 128) * 512; };
+    const size_t per_block = align_up(3 * sq, 1024) + align_up(sq, 1024) + align_up(2 * (size_t)kFfn * kHidden, 1024) +
+                             align_up((size_t)kHidden * kFfn, 1024) + align_up(sf_bytes(3 * kHidden, kHidden), 1024) +
+                             align_up(sf_bytes(kHidden, kHidden), 1024) +
+                             align_up(sf_bytes(2 * kFfn, kHidden), 1024) + align_up(sf_bytes(kHidden, kFfn), 1024);
+    const size_t act = align_up(R * kFfn, 1024) + align_up(sf_bytes(R, kFfn), 1024);
+    e = cudaMalloc(&d->mxmem, per_block * cfg->blocks + act);
+    if (e != cudaSuccess) {
+      cudaFree(d->amem);
+      cudaFree(d->wmem);
+      delete d;
+      return fail(QI_ERR_OOM, "qi_dit_create: MXFP8 store: %s", cudaGetErrorString(e));
+    }
+    char* p = static_cast<char*>(d->mxmem);
+    auto take = [&p](size_t n) {
+      uint8_t* r = reinterpret_cast<uint8_t*>(p);
+      p += align_up(n, 1024);
+      return r;
+    };
+    d->bmx.resize(cfg->blocks);
+    for (auto& b : d->bmx) {
+      b.wqkv = take(3 * sq);
+      b.wo = take(sq);
+      b.wgu = take(2 * (size_t)kFfn * kHidden);
+      b.wd = take((size_t)kHidden * kFfn);
+      b.sqkv = take(sf_bytes(3 * kHidden, kHidden));
+      b.so = take(sf_bytes(kHidden, kHidden));
+      b.sgu = take(sf_bytes(2 * kFfn, kHidden));
+      b.sd = take(sf_bytes(kHidden, kFfn));
+    }
+    d->aq = take(R * kFfn);
+    d->asf = take(sf_bytes(R, kFfn));
+    d->has_mx = true;
+  }
+
   // ---- weight tensor maps (B operands: 256-row boxes)
   qi_status st = make_map(&d->m_txt, d->txt_w, kHidden, kHidden, 256);
   for (int b = 0; st == QI_OK && b < cfg->blocks; ++b) {
@@ -538,8 +625,17 @@ qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out) {
     if (st == QI_OK) st = make_map(&B.m_o, B.wo, kHidden, kHidden, 256);
     if (st == QI_OK) st = make_map(&B.m_gu, B.wgu, 2 * kFfn, kHidden, 256);
     if (st == QI_OK) st = make_map(&B.m_d, B.wd, kHidden, kFfn, 256);
+    if (st == QI_OK && d->has_mx) {
+      auto& M = d->bmx[b];
+      if (!qi::encode_map8(&M.m_qkv, M.wqkv, 3 * kHidden, kHidden, 256) ||
+          !qi::encode_map8(&M.m_o, M.wo, kHidden, kHidden, 256) ||
+          !qi::encode_map8(&M.m_gu, M.wgu, 2 * kFfn, kHidden, 256) ||
+          !qi::encode_map8(&M.m_d, M.wd, kHidden, kFfn, 256))
+        st = fail(QI_ERR_CUDA, "qi_dit_create: 8-bit tensor map encoding failed");
+    }
   }
   if (st != QI_OK) {
+    if (d->mxmem) cudaFree(d->mxmem);
     cudaFree(d->amem);
     cudaFree(d->wmem);
     delete d;
@@ -568,6 +664,7 @@ qi_status qi_dit_destroy(qi_dit* d) {
                  d->fbc_x0, d->fbc_x1, d->fbc_r0[0], d->fbc_r0[1], d->fbc_rest};
   for (float* p : st)
     if (p) cudaFree(p);
+  if (d->mxmem) cudaFree(d->mxmem);
   if (d->fbc_part) cudaFree(d->fbc_part);
   if (d->fbc_out) cudaFree(d->fbc_out);
   cudaFree(d->amem);
@@ -618,6 +715,14 @@ qi_status qi_dit_load_block(qi_dit* d, int block, const qi_block_weights* w, int
   QI_CUDA(cudaMemcpy2DAsync(reinterpret_cast<char*>(B.wgu) + grp, 2 * grp, w->wu, grp, grp, kFfn / (kBN / 2), kind,
                             s));
   QI_CUDA(cudaMemcpyAsync(B.wd, w->wd, (size_t)kHidden * kFfn * 2, kind, s));
+  if (d->has_mx) {
+    // from the bf16 values themselves, before they become fp16
+    auto& M = d->bmx[block];
+    QI_CUDA(qi::launch_quant_mx(B.wqkv, true, 3 * kHidden, kHidden, M.wqkv, M.sqkv, s));
+    QI_CUDA(qi::launch_quant_mx(B.wo, true, kHidden, kHidden, M.wo, M.so, s));
+    QI_CUDA(qi::launch_quant_mx(B.wgu, true, 2 * kFfn, kHidden, M.wgu, M.sgu, s));
+    QI_CUDA(qi::launch_quant_mx(B.wd, true, kHidden, kFfn, M.wd, M.sd, s));
+  }
   QI_TRY(convert_weights(d,
                          {{B.wqkv, 3 * sq}, {B.wo, sq}, {B.wgu, (size_t)2 * kFfn * kHidden}, {B.wd, (size_t)kHidden * kFfn}},
                          s, "qi_dit_load_block"));
@@ -984,6 +1089,52 @@ qi_status qi_gemm_bf16(qi_dit* d, const uint16_t* A, const uint16_t* B, float* D
   g.err = d->err;
   QI_CUDA(cudaSetDevice(d->device));
   QI_CUDA(qi::launch_gemm(qi::kEpiF32, ma, mb, g, d->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+  return QI_OK;
+}
+
+qi_status qi_dit_set_mxfp8(qi_dit* d, int on) {
+  if (!d) return fail(QI_ERR_INVALID_ARG, "qi_dit_set_mxfp8: NULL handle");
+  if (on && !d->has_mx) return fail(QI_ERR_STATE, "qi_dit_set_mxfp8: the handle was created without mxfp8");
+  if (d->mx_on != (on != 0)) {
+    // text K/V and the first-block cache's reference were made by the other arithmetic
+    d->cache_L[0] = d->cache_L[1] = -1;
+    d->fbc_N = -1;
+  }
+  d->mx_on = on != 0;
+  return QI_OK;
+}
+
+qi_status qi_quant_mxfp8(const uint16_t* in, int in_is_bf16, int rows, int K, uint8_t* q, uint8_t* sf,
+                         qi_stream_t stream) {
+  if (!in || !q || !sf) return fail(QI_ERR_INVALID_ARG, "qi_quant_mxfp8: NULL argument");
+  if (rows < 1 || K < 128 || K % 128 != 0) return fail(QI_ERR_SHAPE, "qi_quant_mxfp8: rows %d K %d", rows, K);
+  if ((reinterpret_cast<uintptr_t>(in) & 15) || (reinterpret_cast<uintptr_t>(q) & 15))
+    return fail(QI_ERR_INVALID_ARG, "qi_quant_mxfp8: in and q must be 16-byte aligned");
+  QI_CUDA(qi::launch_quant_mx(in, in_is_bf16 != 0, rows, K, q, sf, reinterpret_cast<cudaStream_t>(stream)));
+  return QI_OK;
+}
+
+qi_status qi_gemm_mxfp8(qi_dit* d, const uint8_t* A, const uint8_t* A_sf, const uint8_t* B, const uint8_t* B_sf,
+                        float* D, int M, int N, int K, qi_stream_t stream) {
+  if (!d || !A || !A_sf || !B || !B_sf || !D) return fail(QI_ERR_INVALID_ARG, "qi_gemm_mxfp8: NULL argument");
+  if (M < 1 || N < kBN || N % kBN != 0 || K < 128 || K % 128 != 0)
+    return fail(QI_ERR_SHAPE, "qi_gemm_mxfp8: M %d N %d K %d", M, N, K);
+  if ((reinterpret_cast<uintptr_t>(A_sf) & 15) || (reinterpret_cast<uintptr_t>(B_sf) & 15) ||
+      (reinterpret_cast<uintptr_t>(D) & 15))
+    return fail(QI_ERR_INVALID_ARG, "qi_gemm_mxfp8: scale chunks and D must be 16-byte aligned");
+  CUtensorMap ma, mb;
+  if (!qi::encode_map8(&ma, A, M, K, 128) || !qi::encode_map8(&mb, B, N, K, 256))
+    return fail(QI_ERR_INVALID_ARG, "qi_gemm_mxfp8: tensor map encoding failed (alignment?)");
+  qi::GemmParams g{};
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.d = D;
+  g.err = d->err;
+  g.sfa = A_sf;
+  g.sfb = B_sf;
+  QI_CUDA(cudaSetDevice(d->device));
+  QI_CUDA(qi::launch_gemm_mx(qi::kEpiF32, ma, mb, g, d->num_sms, reinterpret_cast<cudaStream_t>(stream)));
   return QI_OK;
 }
 

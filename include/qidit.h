@@ -95,6 +95,9 @@ typedef struct qi_dit_config {
   int N_max;  /* largest image token count this handle serves (1..16384)        */
   int kv_slots; /* text K/V slots: 0 or 1 = one; 2 = a second slot for the negative
                  * prompt of classifier-free guidance (qi_dit_step_cfg)          */
+  int mxfp8;    /* 1 = also keep MXFP8 copies of the block weights (+7.1 GB at 32
+                 * blocks) so that passes can run on block-scaled GEMMs
+                 * (qi_dit_set_mxfp8); 0 = fp16 only                             */
 } qi_dit_config;
 
 /* Global (non-block) tensors, bf16 bits, [out, in] row-major. */
@@ -327,6 +330,41 @@ qi_status qi_dit_read_kv(qi_dit* dit, int block, int row0, int rows, uint16_t* k
  * Uses the handle's device error word. Errors: SHAPE, INVALID_ARG, CUDA. */
 qi_status qi_gemm_bf16(qi_dit* dit, const uint16_t* A, const uint16_t* B, float* D, int M, int N, int K,
                        qi_stream_t stream);
+
+/* ------------------------------------------------------------------ MXFP8 */
+
+/* Block-scaled low-precision GEMMs [MLX page: 4-bit quantised weights, an int8
+ * "per_block 32" experiment; Core AI page: int8 / 4-bit weight quantisation].
+ * GB300 reading: OCP MX v1.0 MXFP8, i.e. blocks of 32 consecutive values along
+ * the contraction axis share one scale 2^e (UE8M0 byte e + 127) and each value
+ * is FP8 E4M3; e = floor(log2 max|v|) - 8 clamped to [-127, 127] (-127 for an
+ * all-zero block), v * 2^-e rounded to nearest even and clamped to +-448.
+ *
+ * qi_dit_set_mxfp8: on = 1 runs the four block GEMMs of every later pass (QKV,
+ * out-projection, gate/up, down) on MXFP8 weights (quantised from the bf16
+ * values at load) and MXFP8 activations (quantised from the fp16 operands just
+ * before each GEMM); the pre-norm GEMMs quantise x * (1 + s) and scale the product
+ * by the row's 1/rms. on = 0 returns to fp16. Switching drops the text K/V
+ * captures and the first-block cache's reference. Host only.
+ * Errors: INVALID_ARG (NULL), STATE (handle created with mxfp8 = 0). */
+qi_status qi_dit_set_mxfp8(qi_dit* dit, int on);
+
+/* MXFP8 quantisation along K of a row-major [rows, K] 16-bit matrix (bf16 bits
+ * if in_is_bf16, else fp16; device, 16-byte aligned): q [rows, K] E4M3 bytes
+ * (device, 16-byte aligned) and sf, the scales in 512-byte chunks, chunk
+ * (K-group k / 128, row group r / 128) at ((k / 128) * ceil(rows / 128) + r / 128) * 512,
+ * byte (r % 32) * 16 + ((r % 128) / 32) * 4 + (k / 32) % 4 within it; sf holds
+ * ceil(rows / 128) * (K / 128) * 512 bytes (bytes of rows past `rows` are left
+ * as they were). Errors: INVALID_ARG, SHAPE (K % 128 != 0). */
+qi_status qi_quant_mxfp8(const uint16_t* in, int in_is_bf16, int rows, int K, uint8_t* q, uint8_t* sf,
+                         qi_stream_t stream);
+
+/* The block-scaled GEMM on its own (test hook): D[M, N] = A[M, K] * B[N, K]^T,
+ * fp32 out, with A, B and their scales as qi_quant_mxfp8 writes them (device).
+ * Requires N % 256 == 0, K % 128 == 0. Uses the handle's device error word.
+ * Errors: SHAPE, INVALID_ARG, CUDA. */
+qi_status qi_gemm_mxfp8(qi_dit* dit, const uint8_t* A, const uint8_t* A_sf, const uint8_t* B,
+                        const uint8_t* B_sf, float* D, int M, int N, int K, qi_stream_t stream);
 
 /* qi_gemm_bf16 without a handle and without allocating. The pages have no
  * counterpart: this exists for callers that may not call the CUDA allocator,

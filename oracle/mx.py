@@ -56,17 +56,16 @@ def e4m3_round(q: np.ndarray) -> np.ndarray:
     """Round float64 values to the nearest E4M3 value (ties to even), clamping at +-448."""
     q = np.asarray(q, np.float64)
     a = np.abs(q)
-    with np.errstate(divide="ignore"):
-        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
-    e = np.maximum(e, E4M3_EMIN)
-    ulp = np.exp2(e - 3)
-    r = np.round(a / ulp) * ulp                  # numpy rounds halves to even
+    _, E = np.frexp(a)                           # a = f * 2^E, f in [0.5, 1): floor(log2 a) = E - 1
+    shift = np.maximum(E - 1, E4M3_EMIN) - 3     # log2 of the E4M3 spacing at a
+    r = np.ldexp(np.round(np.ldexp(a, -shift)), shift)   # exact scalings; round() is half-to-even
     r = np.minimum(r, E4M3_MAX)
     return np.copysign(r, q)
 
 
 def e4m3_encode(v: np.ndarray) -> np.ndarray:
-    """Byte codes of values that are exactly E4M3 (as produced by e4m3_round)."""
+    """Byte codes of values that are exactly E4M3 (as produced by e4m3_round); rounding
+    keeps the sign, so a negative value that rounds to zero is -0 (0x80)."""
     v = np.asarray(v, np.float64)
     finite = E4M3_TABLE.copy()
     finite[np.isnan(finite)] = np.inf
@@ -76,8 +75,7 @@ def e4m3_encode(v: np.ndarray) -> np.ndarray:
     idx = np.minimum(idx, 126)
     code = order[idx].astype(np.uint8)
     assert np.array_equal(E4M3_TABLE[code], np.abs(v)), "value is not an E4M3 number"
-    neg = (np.signbit(v)) & (v != 0)
-    return np.where(neg, code | 0x80, code).astype(np.uint8)
+    return np.where(np.signbit(v), code | 0x80, code).astype(np.uint8)   # -0 keeps its sign: 0x80
 
 
 def shared_exponent(block_amax: np.ndarray) -> np.ndarray:

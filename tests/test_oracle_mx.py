@@ -79,10 +79,11 @@ def test_exact_round_trip_and_error_bound():
 
 
 def test_encode_decodes_back():
-    vals = np.array([0.0, 1.0, -2.5, 448.0, -448.0, 2.0 ** -9, -(2.0 ** -6)])
+    vals = np.array([0.0, 1.0, -2.5, 448.0, -448.0, 2.0 ** -9, -(2.0 ** -6), -0.0])
     codes = mx.e4m3_encode(vals)
     assert np.array_equal(mx.E4M3_TABLE[codes], vals)
-    assert codes.tolist() == [0x00, 0x38, 0xC2, 0x7E, 0xFE, 0x01, 0x88]
+    assert codes.tolist() == [0x00, 0x38, 0xC2, 0x7E, 0xFE, 0x01, 0x88, 0x80]
+    assert mx.e4m3_encode(mx.e4m3_round(np.array([-1e-5]))).tolist() == [0x80]
 
 
 def test_mx_linear_is_the_dequantized_product():
@@ -146,3 +147,83 @@ def test_control_planted_quantiser_mistakes(bad, monkeypatch):
         mids = (pos[:-1] + pos[1:]) / 2
         evens = np.where(np.arange(126) % 2 == 0, pos[:-1], pos[1:])
         assert not np.array_equal(mx.e4m3_round(mids), evens)
+
+
+# ----------------------------------------------------------------------------- tolerance
+# The library quantises the fp16 copies of its GEMM inputs and runs attention on fp16
+# Q / K / V. Rounding a value to fp16 moves it by <= 2^-11 relative, which carries about
+# 2^-7 of the E4M3 codes one step (2^-3 relative) away from the float32 oracle's code. The
+# GPU tests of the MXFP8 mode use the tolerance below; this test shows that those fp16
+# roundings alone, emulated here in numpy on the one-block workload, already use most of it.
+MX_BLOCK_COS, MX_BLOCK_REL = 0.999, 5e-2
+
+
+def _f16(a):
+    return np.asarray(a, np.float32).astype(np.float16).astype(np.float32)
+
+
+def _block_fp16_operands(bw, x, mods, L, cos, sin, heads):
+    """oracle/mx.block_forward with every quantiser input and Q / K / V rounded to fp16."""
+    R, H = x.shape
+    D = H // heads
+    s1, g1, s2, g2 = dit.mod_chunks(mods)
+    xm = _f16(x * (np.float32(1.0) + s1))
+    r1 = mx._rinv(x)
+    q = _f16((r1 * mx.mx_linear(xm, bw["wq"])).reshape(R, heads, D))
+    k = (r1 * mx.mx_linear(xm, bw["wk"])).reshape(R, heads, D)
+    v = _f16((r1 * mx.mx_linear(xm, bw["wv"])).reshape(R, heads, D))
+    q, k = _f16(dit.rope(q, cos, sin)), _f16(dit.rope(k, cos, sin))
+    o = _f16(mx.attention_masked(q, k, v, L))
+    x = (x + g1 * mx.mx_linear(o, bw["wo"])).astype(np.float32)
+    xm2 = _f16(x * (np.float32(1.0) + s2))
+    r2 = mx._rinv(x)
+    h = _f16(dit.silu(r2 * mx.mx_linear(xm2, bw["wg"])) * (r2 * mx.mx_linear(xm2, bw["wu"])))
+    return (x + g2 * mx.mx_linear(h, bw["wd"])).astype(np.float32)
+
+
+@pytest.mark.slow
+def test_fp16_operand_roundings_fit_the_mxfp8_tolerance():
+    case = synth.BLOCK_CASE
+    W = synth.Weights(seed=case.seed, nblocks=1)
+    x = synth.block_hidden(case)
+    tc, ts, ic, is_ = rope.token_tables(case.L, case.h, case.w)
+    cos, sin = np.concatenate([tc, ic]), np.concatenate([ts, is_])
+    mods = dit.row_mods(dit.modulation(W.glob, case.timestep), dit.modulation(W.glob, 0.0), case.L,
+                        case.L + case.N)
+    bw = W.block(0)
+    ref = mx.block_forward(bw, x, mods, case.L, cos, sin, 32) - x
+    emu = _block_fp16_operands(bw, x, mods, case.L, cos, sin, 32) - x
+    f32 = dit.block_forward(bw, x, mods, case.L, cos, sin, 32) - x
+    row_cos = (emu * ref).sum(1) / np.linalg.norm(emu, axis=1) / np.linalg.norm(ref, axis=1)
+    rel = np.abs(emu - ref).max() / np.abs(ref).max()
+    assert row_cos.min() >= MX_BLOCK_COS and rel <= MX_BLOCK_REL
+    assert rel > 0.3 * MX_BLOCK_REL                        # the roundings use a real share of it
+    # and the emulation stays much closer to the MXFP8 block than that is to float32
+    assert np.sqrt(((emu - ref) ** 2).mean()) < 0.75 * np.sqrt(((ref - f32) ** 2).mean())
+
+
+MX_STEP_COS, MX_STEP_REL = 0.99, 1e-1   # two blocks and the output head (256^2 workload)
+
+
+@pytest.mark.slow
+def test_fp16_operand_roundings_fit_the_mxfp8_step_tolerance():
+    case = synth.STEP_256
+    nb = 2
+    W = synth.Weights(seed=case.seed, nblocks=nb)
+    img = synth.img_tokens(case)
+    txt = synth.txt_feats(case)
+    tabs = rope.token_tables(case.L, case.h, case.w)
+    t = np.float32(case.timestep)
+    ref = mx.dit_forward(W, img, txt, t, *tabs, nblocks=nb)
+    g = W.glob
+    L = case.L
+    mods = dit.row_mods(dit.modulation(g, t), dit.modulation(g, 0.0), L, L + case.N)
+    cos = np.concatenate([tabs[0], tabs[2]])
+    sin = np.concatenate([tabs[1], tabs[3]])
+    x = dit.embed(g, img, txt)
+    for b in range(nb):
+        x = _block_fp16_operands(W.block(b), x, mods, L, cos, sin, 32)
+    emu = dit.head(g, x[L:])
+    row_cos = (emu * ref).sum(1) / np.linalg.norm(emu, axis=1) / np.linalg.norm(ref, axis=1)
+    rel = np.abs(emu - ref).max() / np.abs(ref).max()
+    assert row_cos.min() >= MX_STEP_COS and rel <= MX_STEP_REL
