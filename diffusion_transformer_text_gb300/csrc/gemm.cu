@@ -11,8 +11,10 @@
 // (r % 32) * 16 + ((r % 128) / 32) * 4 + k) ordered [K / 128][rows / 128]. A
 // stage then covers K = 128; its scale chunks arrive by bulk copy with the
 // tiles, are copied into a per-stage set of TMEM columns (tcgen05.cp) and feed
-// four block-scaled MMAs (K = 32 each, the scale byte chosen per MMA). The scale
-// columns leave room for one 256-column accumulator only.
+// four block-scaled MMAs (K = 32 each, the scale byte chosen per MMA). The two
+// 256-column accumulators fill tensor memory, so a tile keeps its scales in the
+// first 64 columns of the other accumulator: written only after the previous
+// tile's MMAs have completed and its epilogue has read those columns.
 //
 // Roles per CTA (192 threads):
 //   warp 0     TMA producer: 128x64 A and 256x64 B tiles into a 4-stage ring
@@ -44,10 +46,11 @@ struct Geo {
   static constexpr int kSF = MX ? 3 * kSfChunk : 0;
   static constexpr int kStage = kABytes + kBBytes + kSF;
   static constexpr int kK = MX ? 128 : kBK;  // K elements per stage
-  static constexpr int kAcc = MX ? 1 : 2;    // TMEM accumulators
+  static constexpr int kAcc = 2;             // TMEM accumulators (256 columns each)
   static constexpr int kSmem = kStages * kStage + 1024 + 256 + kEpiScratch;
 };
-constexpr uint32_t kSfCol = 256;  // MXFP8: stage s scales at columns 256 + 16 s (A: +0..3, B: +4..11)
+// MXFP8: a tile's stage-s scales sit at columns 16 s (A: +0..3, B: +4..11) of the OTHER
+// accumulator, i.e. inside the tile the epilogue is draining.
 // fp16 operands for the DiT epilogues, bf16 for the plain fp32 test hook
 template <int KIND>
 constexpr uint32_t kIdesc = KIND == kEpiF32 ? idesc_bf16_f32(kBM, kBN) : idesc_f16_f32(kBM, kBN);
@@ -93,7 +96,17 @@ __device__ __forceinline__ void store_f16x32(act_t* dst, const float (&v)[32]) {
 
 // ---------------------------------------------------------------- epilogues
 
-__device__ __forceinline__ void epi_qkv(const GemmParams& p, uint32_t taddr, int row, int n0) {
+// MXFP8: the next tile's scale sets go into the first 64 columns of the
+// accumulator this epilogue drains; once every epilogue warp has read them
+// (chunks 0 and 1 of 32 columns) the warp tells the MMA issuer.
+__device__ __forceinline__ void release_sf_cols(uint64_t* sf_bar, int c) {
+  if (sf_bar == nullptr || c != 1) return;
+  tc_fence_before();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(sf_bar);
+}
+
+__device__ __forceinline__ void epi_qkv(const GemmParams& p, uint32_t taddr, int row, int n0, uint64_t* sf_bar) {
   const bool valid = row < p.M;
   float rinv = 0.f;
   const float* cs = nullptr;
@@ -117,6 +130,7 @@ __device__ __forceinline__ void epi_qkv(const GemmParams& p, uint32_t taddr, int
     uint32_t r[32];
     tmem_ld32(taddr + c * 32, r);
     tmem_ld_wait();
+    release_sf_cols(sf_bar, c);
     if (!valid) continue;
     float v[32];
 #pragma unroll
@@ -151,7 +165,7 @@ __device__ __forceinline__ void epi_qkv(const GemmParams& p, uint32_t taddr, int
 // the row's sum of squares over the tile's 256 columns is accumulated per lane
 // and reduced per row in a fixed order.
 __device__ __forceinline__ void epi_resid(const GemmParams& p, uint32_t taddr, int row0, int lane, int n0,
-                                          float* sm) {
+                                          float* sm, uint64_t* sf_bar) {
   float sq[32];
 #pragma unroll
   for (int rr = 0; rr < 32; ++rr) sq[rr] = 0.f;
@@ -160,6 +174,7 @@ __device__ __forceinline__ void epi_resid(const GemmParams& p, uint32_t taddr, i
     uint32_t r[32];
     tmem_ld32(taddr + c * 32, r);
     tmem_ld_wait();
+    release_sf_cols(sf_bar, c);
 #pragma unroll
     for (int k = 0; k < 32; ++k) sm[lane * 33 + k] = __uint_as_float(r[k]);
     __syncwarp();
@@ -203,7 +218,8 @@ __device__ __forceinline__ void epi_resid(const GemmParams& p, uint32_t taddr, i
   if (row0 + lane < p.M) p.ssp_out[static_cast<size_t>(row0 + lane) * kSspParts + n0 / kBN] = ss;
 }
 
-__device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, int row, int n0) {
+__device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, int row, int n0,
+                                           uint64_t* sf_bar) {
   const bool valid = row < p.M;
   const float rinv = valid ? row_rinv(p.ssp_in, row) : 0.f;
   // tile columns [0,128) are gate rows 128j.., [128,256) the matching up rows
@@ -214,6 +230,7 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, 
     tmem_ld32(taddr + c * 32, g);
     tmem_ld32(taddr + kBN / 2 + c * 32, u);
     tmem_ld_wait();
+    release_sf_cols(sf_bar, c);
     if (!valid) continue;
     float hv[32];
 #pragma unroll
@@ -226,7 +243,7 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, 
   }
 }
 
-__device__ __forceinline__ void epi_f32(const GemmParams& p, uint32_t taddr, int row, int n0) {
+__device__ __forceinline__ void epi_f32(const GemmParams& p, uint32_t taddr, int row, int n0, uint64_t* sf_bar) {
   const bool valid = row < p.M;
   float* dst = p.d + static_cast<size_t>(row) * p.N + n0;
 #pragma unroll 1
@@ -234,6 +251,7 @@ __device__ __forceinline__ void epi_f32(const GemmParams& p, uint32_t taddr, int
     uint32_t r[32];
     tmem_ld32(taddr + c * 32, r);
     tmem_ld_wait();
+    release_sf_cols(sf_bar, c);
     if (!valid) continue;
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -260,7 +278,8 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sffree = drain + 1;  // MXFP8: scale columns of accumulator a readable again
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sffree + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -278,6 +297,7 @@ __global__ void __launch_bounds__(192, 1)
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], 4);
+      mbar_init(&sffree[a], 4);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -340,12 +360,23 @@ __global__ void __launch_bounds__(192, 1)
       // ---------------- MMA issuer
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+      int local = 0;  // tiles this CTA has issued
+      for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++local) {
         if (*abort_flag) break;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u)) {
           report_error(p.err, kErrTimeoutMma);
           *abort_flag = 1;
           break;
+        }
+        if (MX && local > 0) {
+          // the previous tile (other accumulator) must be complete, and its epilogue
+          // past the first 64 columns, before this tile's scales go there
+          const uint32_t prev_parity = static_cast<uint32_t>((local - 1) >> 1) & 1u;
+          if (!mbar_wait(&tfull[acc ^ 1u], prev_parity) || !mbar_wait(&sffree[acc ^ 1u], prev_parity)) {
+            report_error(p.err, kErrTimeoutMma);
+            *abort_flag = 1;
+            break;
+          }
         }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * kBN;
@@ -362,7 +393,7 @@ __global__ void __launch_bounds__(192, 1)
           if (MX) {
             // this stage's scale set: the MMAs that last read it (kStages stages ago)
             // completed before the producer could refill the stage
-            const uint32_t sf_t = tmem_base + kSfCol + 16 * stage;
+            const uint32_t sf_t = tmem_base + (acc ^ 1u) * kBN + 16 * stage;
             const uint32_t sf_s = smem_u32(sSF + stage * G::kSF);
             tmem_cp_sf(sf_t, plain_rows16_desc(sf_s));
             tmem_cp_sf(sf_t + 4, plain_rows16_desc(sf_s + kSfChunk));
@@ -412,15 +443,16 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN;
       const int row = mt * kBM + row_in_tile;
+      uint64_t* sf_bar = MX ? &sffree[acc] : nullptr;
       if (KIND == kEpiQkv)
-        epi_qkv(p, taddr, row, nt * kBN);
+        epi_qkv(p, taddr, row, nt * kBN, sf_bar);
       else if (KIND == kEpiResid)
         epi_resid(p, taddr, mt * kBM + quarter * 32, lane, nt * kBN,
-                  reinterpret_cast<float*>(smem + kStages * G::kStage + 256) + (warp - 2) * 32 * 33);
+                  reinterpret_cast<float*>(smem + kStages * G::kStage + 256) + (warp - 2) * 32 * 33, sf_bar);
       else if (KIND == kEpiSwiglu)
-        epi_swiglu(p, taddr, row, nt * kBN);
+        epi_swiglu(p, taddr, row, nt * kBN, sf_bar);
       else
-        epi_f32(p, taddr, row, nt * kBN);
+        epi_f32(p, taddr, row, nt * kBN, sf_bar);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);

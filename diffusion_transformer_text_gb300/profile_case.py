@@ -1,6 +1,6 @@
 """A small DiT case for profiler captures (same kernels and shapes per launch as 1024^2).
 
-    python -m diffusion_transformer_text_gb300.profile_case [--blocks 2] [--steps 2] [--N 4096] [--L 407]
+    python -m diffusion_transformer_text_gb300.profile_case [--blocks 2] [--steps 2] [--N 4096] [--L 407] [--mxfp8]
 
 Builds a handle with `blocks` blocks of random-init bf16 weights drawn on the
 device, runs one joint step (text K/V capture) and then `steps` image-only
@@ -8,7 +8,8 @@ steps at N image tokens and L text rows, and prints the wall time. With two
 blocks it holds about 1.5 GB on the device (weights alone exceed the L2), so a
 full profiler capture of one launch stays small. Launch order per pass: text
 GEMM (joint only), then per block QKV GEMM, attention, out-projection GEMM,
-gate/up GEMM, down GEMM.
+gate/up GEMM, down GEMM. With --mxfp8 the block GEMMs run on MXFP8 operands
+(an activation quantiser launch before each of them).
 """
 from __future__ import annotations
 
@@ -29,12 +30,13 @@ def main():
     ap.add_argument("--steps", type=int, default=2)
     ap.add_argument("--N", type=int, default=4096)
     ap.add_argument("--L", type=int, default=407)
+    ap.add_argument("--mxfp8", action="store_true")
     a = ap.parse_args()
     h = w = int(round(a.N ** 0.5))
     assert h * w == a.N, "N must be a square grid"
     qi.build()
     dev = torch.device("cuda", 0)
-    d = qi.DiT(blocks=a.blocks, L_max=a.L, N_max=a.N)
+    d = qi.DiT(blocks=a.blocks, L_max=a.L, N_max=a.N, mxfp8=a.mxfp8)
     g = torch.Generator(device=dev)
     g.manual_seed(7)
 
@@ -45,6 +47,7 @@ def main():
     d.load_global({n: t(*s(dims)) for n, s, _ in synth.GLOBAL_TENSORS})
     for b in range(a.blocks):
         d.load_block(b, {n: t(*s(dims)) for n, s, _ in synth.BLOCK_TENSORS})
+    d.set_mxfp8(a.mxfp8)
     tc, ts, ic, is_ = qi.rope_tables(a.L, h, w)
     txt = torch.randn(a.L, 4096, generator=g, device=dev)
     x = torch.randn(a.N, 64, generator=g, device=dev)
@@ -56,7 +59,7 @@ def main():
         vel = d.step_cached(x, a.L, float(np.float32(tsteps[i]) / np.float32(1000)), ic, is_, vel=vel)
     torch.cuda.synchronize()
     d.check()
-    print(f"profile case: blocks {a.blocks}, N {a.N}, L {a.L}, 1 joint + {a.steps} image-only steps, "
+    print(f"profile case: blocks {a.blocks}, N {a.N}, L {a.L}, mxfp8 {a.mxfp8}, 1 joint + {a.steps} image-only steps, "
           f"{(time.perf_counter() - t0) * 1e3:.1f} ms")
     d.close()
 
