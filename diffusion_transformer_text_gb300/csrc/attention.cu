@@ -4,20 +4,28 @@
 //   (i < L and j <= i)  -- text rows are causal over text only
 //   (i >= L and j < Lk) -- image rows see every text and image key.
 // This is the port's "two SDPA calls" decomposition (text->text causal,
-// image->all) done in one pass. Keys are visited in 128-row tiles from key 0 in
+// image->all) done in one pass. Keys are visited in 64-row tiles from key 0 in
 // the same order whatever the query tile holds, so an image row's result is the
 // same in a joint pass and in an image-only pass over the stored text K/V.
 //
 // CTA = 128 query rows of one head; two CTAs share an SM (256 TMEM columns and
-// ~98 KB of shared memory each), so one CTA's softmax overlaps the other's MMAs.
-// Roles (192 threads):
-//   warp 0     TMA producer: Q once, then K and V tiles (128 keys x 128 dims)
-//   warp 1     TMEM owner and MMA issuer: S = Q K^T (M128 N128, both K-major),
-//              then O += P V with P read from TMEM and V MN-major in shared memory
+// ~98 KB of shared memory each). Keys come in 64-row tiles and S is double
+// buffered in tensor memory, so the MMA warp computes S(j+1) = Q K(j+1)^T while
+// the softmax warps turn S(j) into P(j):
+//   TMEM columns [0,64) S buffer 0, [64,128) S buffer 1, [128,256) O.
+// Roles (224 threads):
+//   warp 0     TMA producer of Q (once) and the K tiles (64 keys x 128 dims, two
+//              slots); warp 6 produces the V tiles (two slots). Separate threads,
+//              so a K load never queues behind a V slot that PV still reads.
+//   warp 1     TMEM owner and MMA issuer, in the order S(0), S(1), PV(0), S(2),
+//              PV(1), ...: S(j+1) = Q K^T (M128 N64, both K-major) once PV(j-1)
+//              has read the P that shared its buffer; O += P(j) V(j) with P read
+//              from TMEM and V MN-major in shared memory
 //   warps 2-5  softmax: thread = query row (TMEM lane). Reads its S row, keeps a
 //              running max (O is rescaled only when the max grows by more than
-//              2^8, the row sum uses the same max, so the result is unchanged),
-//              writes P as fp16 over the S columns, and at the end scales O by
+//              2^8 -- after the previous PV has landed -- and the row sum uses the
+//              same max, so the result is unchanged), writes P as fp16 over the
+//              first 32 columns of the S buffer, and at the end scales O by
 //              1 / rowsum and stores it.
 // Every mbarrier wait is bounded; on expiry the error word is set and the CTA
 // drains its copies and MMAs before releasing TMEM.
@@ -28,34 +36,40 @@ namespace qi {
 namespace {
 
 constexpr int kBQ = 128;                       // query rows per CTA
-constexpr int kBKV = 128;                      // keys per tile
-constexpr int kHalfBytes = 128 * 64 * 2;       // one 128-row x 64-column swizzled box: 16 KB
-constexpr int kTileBytes = 2 * kHalfBytes;     // 128 rows x 128 dims: 32 KB
-constexpr int kSmem = 3 * kTileBytes + 1024 + 256;
-constexpr uint32_t kTmemCols = 256;            // S/P: columns [0,128), O: [128,256)
-constexpr uint32_t kIdescQK = idesc_f16_f32(128, 128);
+constexpr int kBKV = 64;                       // keys per tile
+constexpr int kQHalf = 128 * 64 * 2;           // Q: 128 rows x 64 dims, one swizzled box (16 KB)
+constexpr int kQBytes = 2 * kQHalf;            // Q: 128 rows x 128 dims (32 KB)
+constexpr int kKVHalf = kBKV * 64 * 2;         // K or V: 64 rows x 64 dims (8 KB)
+constexpr int kKVBytes = 2 * kKVHalf;          // K or V tile: 64 rows x 128 dims (16 KB)
+constexpr int kSmem = kQBytes + 4 * kKVBytes + 1024 + 256;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kOCol = 128;
+constexpr uint32_t kIdescQK = idesc_f16_f32(128, kBKV);
 constexpr uint32_t kIdescPV = idesc_f16_f32_bmn(128, 128);
 constexpr float kRescaleLog2 = 8.0f;           // rescale O only when the max grows by > 2^8
 
-__global__ void __launch_bounds__(192, 2)
+constexpr int kThreads = 224;
+
+__global__ void __launch_bounds__(kThreads, 2)
     attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
             const __grid_constant__ CUtensorMap tmV, const AttnParams p, float scale_log2) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
-  uint8_t* sK = smem + kTileBytes;
-  uint8_t* sV = smem + 2 * kTileBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 3 * kTileBytes);
+  uint8_t* sK = smem + kQBytes;                 // two slots
+  uint8_t* sV = sK + 2 * kKVBytes;              // two slots
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + 2 * kKVBytes);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = bars + 2;
-  uint64_t* v_full = bars + 3;
-  uint64_t* v_empty = bars + 4;
-  uint64_t* s_full = bars + 5;
-  uint64_t* p_full = bars + 6;
-  uint64_t* o_done = bars + 7;
-  uint64_t* drain = bars + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
+  uint64_t* k_full = bars + 1;    // [2]
+  uint64_t* k_empty = bars + 3;   // [2]
+  uint64_t* v_full = bars + 5;    // [2]
+  uint64_t* v_empty = bars + 7;   // [2]
+  uint64_t* s_full = bars + 9;    // [2]
+  uint64_t* p_full = bars + 11;   // [2], one arrival per softmax warp
+  uint64_t* pv_done = bars + 13;  // one phase per tile
+  uint64_t* drain = bars + 14;
+  constexpr int kBars = 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -71,7 +85,7 @@ __global__ void __launch_bounds__(192, 2)
   const int ntiles = (kend + kBKV - 1) / kBKV;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 9; ++i) mbar_init(&bars[i], i == 6 ? 4 : 1);
+    for (int i = 0; i < kBars; ++i) mbar_init(&bars[i], (i == 11 || i == 12) ? 4 : 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -88,80 +102,92 @@ __global__ void __launch_bounds__(192, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;        // S (fp32) and, over its first 64 columns, P (fp16 pairs)
-  const uint32_t tO = tmem + 128;  // O accumulator
+  const uint32_t tO = tmem + kOCol;
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 6) {
     if (lane == 0) {
-      // ---------------- TMA producer
-      int k_last = -1, v_last = -1;  // last tile whose K / V load was issued
-      mbar_arrive_expect_tx(q_full, kTileBytes);
-      tma_load_2d(sQ, &tmQ, q_full, col0, r0);
-      tma_load_2d(sQ + kHalfBytes, &tmQ, q_full, col0 + 64, r0);
+      // ---------------- TMA producers: warp 0 Q and K, warp 6 V
+      const bool is_k = warp == 0;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      uint8_t* dst = is_k ? sK : sV;
+      const CUtensorMap* map = is_k ? &tmK : &tmV;
+      int last[2] = {-1, -1};  // last tile whose load was issued, per slot
+      if (is_k) {
+        mbar_arrive_expect_tx(q_full, kQBytes);
+        tma_load_2d(sQ, &tmQ, q_full, col0, r0);
+        tma_load_2d(sQ + kQHalf, &tmQ, q_full, col0 + 64, r0);
+      }
       for (int j = 0; j < ntiles; ++j) {
         if (*abort_flag) break;
-        const uint32_t par = j & 1;
-        if (!mbar_wait(k_empty, par ^ 1u)) {
+        const int slot = j & 1;
+        if (!mbar_wait(&empty[slot], ((j >> 1) & 1) ^ 1u)) {
           report_error(p.err, kErrTimeoutProducer);
           *abort_flag = 1;
           break;
         }
-        mbar_arrive_expect_tx(k_full, kTileBytes);
-        tma_load_2d(sK, &tmK, k_full, col0, j * kBKV);
-        tma_load_2d(sK + kHalfBytes, &tmK, k_full, col0 + 64, j * kBKV);
-        k_last = j;
-        if (!mbar_wait(v_empty, par ^ 1u)) {
-          report_error(p.err, kErrTimeoutProducer);
-          *abort_flag = 1;
-          break;
-        }
-        mbar_arrive_expect_tx(v_full, kTileBytes);
-        tma_load_2d(sV, &tmV, v_full, col0, j * kBKV);
-        tma_load_2d(sV + kHalfBytes, &tmV, v_full, col0 + 64, j * kBKV);
-        v_last = j;
+        mbar_arrive_expect_tx(&full[slot], kKVBytes);
+        tma_load_2d(dst + slot * kKVBytes, map, &full[slot], col0, j * kBKV);
+        tma_load_2d(dst + slot * kKVBytes + kKVHalf, map, &full[slot], col0 + 64, j * kBKV);
+        last[slot] = j;
       }
       // every load this thread issued must land before the CTA may exit
-      if (!mbar_wait(q_full, 0)) report_error(p.err, kErrTimeoutDrain);
-      if (k_last >= 0 && !mbar_wait(k_full, k_last & 1)) report_error(p.err, kErrTimeoutDrain);
-      if (v_last >= 0 && !mbar_wait(v_full, v_last & 1)) report_error(p.err, kErrTimeoutDrain);
+      if (is_k && !mbar_wait(q_full, 0)) report_error(p.err, kErrTimeoutDrain);
+      for (int s2 = 0; s2 < 2; ++s2)
+        if (last[s2] >= 0 && !mbar_wait(&full[s2], (last[s2] >> 1) & 1)) report_error(p.err, kErrTimeoutDrain);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
       bool ok = mbar_wait(q_full, 0);
-      if (!ok) {
-        report_error(p.err, kErrTimeoutMma);
-        *abort_flag = 1;
-      }
       const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV);
-      for (int j = 0; ok && j < ntiles; ++j) {
-        if (*abort_flag) break;
-        const uint32_t par = j & 1;
-        // S may be overwritten once PV of the previous tile has read P
-        if (j > 0 && !mbar_wait(o_done, par ^ 1u)) ok = false;
-        if (ok && !mbar_wait(k_full, par)) ok = false;
-        if (!ok) break;
+      // S(j) = Q K(j)^T into S buffer j % 2
+      auto issue_qk = [&](int j) -> bool {
+        const int slot = j & 1;
+        if (!mbar_wait(&k_full[slot], (j >> 1) & 1)) return false;
         tc_fence_after();
+        const uint32_t kb = k0 + slot * kKVBytes;
+        const uint32_t tS = tmem + static_cast<uint32_t>(slot * kBKV);
 #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k) {
-          const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-          mma_ss(tS, sw128_kmajor_desc(q0 + off), sw128_kmajor_desc(k0 + off), kIdescQK, k > 0 ? 1u : 0u);
+          const uint32_t qoff = (k >> 2) * kQHalf + (k & 3) * 32;
+          const uint32_t koff = (k >> 2) * kKVHalf + (k & 3) * 32;
+          mma_ss(tS, sw128_kmajor_desc(q0 + qoff), sw128_kmajor_desc(kb + koff), kIdescQK, k > 0 ? 1u : 0u);
         }
-        mma_commit(s_full);
-        mma_commit(k_empty);
-        if (!mbar_wait(p_full, par) || !mbar_wait(v_full, par)) {
+        mma_commit(&s_full[slot]);
+        mma_commit(&k_empty[slot]);
+        return true;
+      };
+      if (ok && ntiles > 0) ok = issue_qk(0);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        if (*abort_flag) break;
+        const int slot = j & 1;
+        if (j + 1 < ntiles) {
+          // S buffer (j+1) % 2 held P(j-1): PV(j-1) must have read it
+          if (j >= 1 && !mbar_wait(pv_done, (j - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          if (!issue_qk(j + 1)) {
+            ok = false;
+            break;
+          }
+        }
+        if (!mbar_wait(&p_full[slot], (j >> 1) & 1) || !mbar_wait(&v_full[slot], (j >> 1) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint32_t tP = tmem + static_cast<uint32_t>(slot * kBKV);
+        const uint32_t vb = v0 + slot * kKVBytes;
 #pragma unroll
         for (int k = 0; k < kBKV / 16; ++k) {
           // P columns: 16 keys = 8 columns of fp16 pairs; V rows: 16 keys = 2 KB
-          mma_ts(tO, tS + k * 8, sw128_mnmajor_desc(v0 + k * 2048, kHalfBytes, 1024), kIdescPV,
-                      (j > 0 || k > 0) ? 1u : 0u);
+          mma_ts(tO, tP + k * 8, sw128_mnmajor_desc(vb + k * 2048, kKVHalf, 1024), kIdescPV,
+                 (j > 0 || k > 0) ? 1u : 0u);
         }
-        mma_commit(o_done);
-        mma_commit(v_empty);
+        mma_commit(pv_done);
+        mma_commit(&v_empty[slot]);
       }
       if (!ok) {
         report_error(p.err, kErrTimeoutMma);
@@ -182,27 +208,28 @@ __global__ void __launch_bounds__(192, 2)
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
-      const uint32_t par = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full, par));
+      const int slot = j & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[slot], (j >> 1) & 1));
       if (!ok) break;
       tc_fence_after();
+      const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(slot * kBKV);
       const int kbase = j * kBKV;
-      // the whole S row of this tile: four loads in flight, one wait
-      uint32_t r[4][32];
+      // the whole S row of this tile: two loads in flight, one wait
+      uint32_t r[2][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, r[c]);
+      for (int c = 0; c < 2; ++c) tmem_ld32(tS + c * 32, r[c]);
       tmem_ld_wait();
       // keys at or past the row's limit become -inf (only tiles that reach a limit)
       if (__any_sync(0xffffffffu, kbase + kBKV > lim)) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (kbase + c * 32 + i >= lim) r[c][i] = 0xff800000u;
       }
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(r[c][i]));
       // the tile's row maximum in base-2 units (scale > 0 keeps the order)
@@ -211,14 +238,18 @@ __global__ void __launch_bounds__(192, 2)
       if (j == 0) {
         m_used = m_new;
       } else {
-        // O holds the sum over earlier tiles (their PV finished before this S was
-        // computed). A row whose maximum grew by more than 2^8 brings O and its
-        // row sum to the new maximum. tcgen05.ld/st must be executed by the whole
-        // warp, so the warp runs them if any row needs it; the other rows scale
-        // by exactly 1 and keep their maximum, so a row's result never depends
-        // on which rows share its warp.
+        // A row whose maximum grew by more than 2^8 brings O and its row sum to the
+        // new maximum, once PV(j-1) -- which may still be adding into O -- is done.
+        // tcgen05.ld/st must be executed by the whole warp, so the warp runs them if
+        // any row needs it; the other rows scale by exactly 1 and keep their
+        // maximum, so a row's result never depends on which rows share its warp.
         const bool mine = m_new > m_used + kRescaleLog2;
         if (__any_sync(0xffffffffu, mine)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           const float alpha = mine ? fast_exp2(m_used - m_new) : 1.0f;
 #pragma unroll 1
           for (int c = 0; c < 8; ++c) {
@@ -235,11 +266,11 @@ __global__ void __launch_bounds__(192, 2)
           }
         }
       }
-      // P = 2^(s * scale - m) as fp16 pairs over the first 64 S columns (masked
-      // keys give 2^-inf = 0). Chunk c of P covers S columns already read.
+      // P = 2^(s * scale - m) as fp16 pairs over the first 32 columns of the S
+      // buffer (masked keys give 2^-inf = 0); those columns were read above.
       float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -248,16 +279,16 @@ __global__ void __launch_bounds__(192, 2)
           rs4[i & 3] += a + b;
           pk[i] = pack_f16x2(a, b);
         }
-        tmem_st16(tS + lane_off + c * 16, pk);
+        tmem_st16(tS + c * 16, pk);
       }
       l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(&p_full[slot]);
     }
     // epilogue: wait for the last PV, O / l -> fp16
-    if (ok && ntiles > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (ntiles - 1) & 1));
+    if (ok && ntiles > 0) ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (ntiles - 1) & 1));
     if (!ok) {
       if (lane == 0) report_error(p.err, kErrTimeoutEpilogue);
       *abort_flag = 1;
@@ -305,12 +336,12 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
     attr_set = true;
   }
   CUtensorMap mq, mk, mv;
-  if (!encode_map16(&mq, p.q, p.Rq, kHidden, 128, false) || !encode_map16(&mk, p.k, p.Lk, kHidden, 128, false) ||
-      !encode_map16(&mv, p.v, p.Lk, kHidden, 128, false))
+  if (!encode_map16(&mq, p.q, p.Rq, kHidden, kBQ, false) || !encode_map16(&mk, p.k, p.Lk, kHidden, kBKV, false) ||
+      !encode_map16(&mv, p.v, p.Lk, kHidden, kBKV, false))
     return cudaErrorInvalidValue;
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kHeadDim));
   dim3 grid((p.Rq + kBQ - 1) / kBQ, kHeads);
-  attn_tc<<<grid, 192, kSmem, stream>>>(mq, mk, mv, p, scale_log2);
+  attn_tc<<<grid, kThreads, kSmem, stream>>>(mq, mk, mv, p, scale_log2);
   return cudaGetLastError();
 }
 
