@@ -287,8 +287,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[slot]);
     }
-    // epilogue: wait for the last PV, O / l -> fp16
-    if (ok && ntiles > 0) ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (ntiles - 1) & 1));
+    // epilogue: O / l -> fp16 once every MMA has completed. With S double-buffered,
+    // PV(n-2) may still be running when the last softmax ends, so a parity wait on
+    // pv_done could match phase n-3; the MMA warp's single-use drain barrier
+    // (committed after its last MMA) cannot.
+    if (ok && ntiles > 0) ok = __all_sync(0xffffffffu, mbar_wait(drain, 0));
     if (!ok) {
       if (lane == 0) report_error(p.err, kErrTimeoutEpilogue);
       *abort_flag = 1;
