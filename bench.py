@@ -462,8 +462,8 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": d2h / e2e_steps},
         "clocks": clk,
         "cfg": {"steps_per_s": world * 1e3 / cfg_ms, "ms_per_step": cfg_ms, "guidance": GUIDE, "neg_tokens": L_NEG,
-                "steps": CFG_STEPS, "note": "two passes per step (conditional + negative prompt), 1 joint + "
-                                            f"{CFG_STEPS - 1} image-only"},
+                "steps": CFG_STEPS, "note": "step 0: two joint passes (each prompt captures its K/V slot); "
+                                            f"{CFG_STEPS - 1} image-only steps: one pass of 2N rows (batch 2)"},
         "dpmpp2m": {"steps_per_s": world * 1e3 / dpm_ms, "ms_per_step": dpm_ms, "steps": DPM_STEPS,
                     "note": "DPM++ 2M update in place of Euler, 1 joint + image-only passes"},
         "fbcache": {"threshold": FB_THR, "steps": FB_STEPS, "skipped": skips, "ms_per_step": fb_ms,

@@ -116,12 +116,16 @@ __device__ __forceinline__ void epi_qkv(const GemmParams& p, uint32_t taddr, int
   const int col_in = n0 - section * kHidden;
   if (valid) {
     rinv = row_rinv(p.ssp_in, row);
-    const bool text = row < p.n_text;
-    const size_t trow = text ? static_cast<size_t>(row) : static_cast<size_t>(row - p.n_text);
-    cs = (text ? p.txt_cos : p.img_cos) + trow * kRopeCols;
-    sn = (text ? p.txt_sin : p.img_sin) + trow * kRopeCols;
+    const bool second = p.split_row > 0 && row >= p.split_row;  // second prompt's image rows
+    const int r = second ? row - p.split_row : row;
+    const bool text = r < p.n_text;
+    const size_t trow = text ? static_cast<size_t>(r) : static_cast<size_t>(r - p.n_text);
+    cs = (text ? p.txt_cos : (second ? p.img_cos2 : p.img_cos)) + trow * kRopeCols;
+    sn = (text ? p.txt_sin : (second ? p.img_sin2 : p.img_sin)) + trow * kRopeCols;
     if (section == 0)
       dst = p.q + static_cast<size_t>(row) * kHidden + col_in;
+    else if (second)
+      dst = (section == 1 ? p.k2 : p.v2) + static_cast<size_t>(r + p.kv_row_off2) * kHidden + col_in;
     else
       dst = (section == 1 ? p.k : p.v) + static_cast<size_t>(row + p.kv_row_off) * kHidden + col_in;
   }

@@ -64,6 +64,15 @@ struct GemmParams {
   const float* txt_sin;
   const float* img_cos;
   const float* img_sin;
+  // two prompts in one pass (guidance): if split_row > 0, rows >= split_row are the
+  // second prompt's image rows: RoPE rows from img_cos2 / img_sin2 and K/V into
+  // k2 / v2 at row (row - split_row) + kv_row_off2
+  int split_row;
+  const float* img_cos2;
+  const float* img_sin2;
+  act_t* k2;
+  act_t* v2;
+  int kv_row_off2;
   // kEpiSwiglu
   act_t* h;
   // kEpiResid

@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -95,6 +96,7 @@ struct qi_dit {
   int device = 0;
   int blocks = 0;
   int L_max = 0, N_max = 0, R_max = 0;
+  int act_rows = 0;  // rows of the activation buffers: R_max, or 2 N_max for two-prompt guidance
   int num_sms = 0;
   bool loaded_global = false;
   std::vector<bool> loaded_block;
@@ -145,8 +147,9 @@ struct qi_dit {
   int slots = 1;           // text K/V slots: 1, or 2 for classifier-free guidance
   int cur_slot = 0;        // slot the running pass reads and writes
   int cache_L[2] = {-1, -1};  // per slot: L of the valid text K/V capture, -1 if none
-  float* vel_pos = nullptr;   // [N_max, 64] guidance: conditional velocity (slots == 2)
-  float* vel_neg = nullptr;   // [N_max, 64] guidance: negative-prompt velocity
+  float* vel_pos = nullptr;   // [2 N_max, 64] guidance: conditional velocity rows, then (batch-2
+                              // passes) the negative prompt's right after them
+  float* vel_neg = nullptr;   // [N_max, 64] guidance: negative-prompt velocity (two-pass joint steps)
 
   // first-block cache, image rows only (allocated on first use)
   float* fbc_x0 = nullptr;            // [N_max, 4096] residual stream entering block 0
@@ -174,7 +177,8 @@ struct qi_dit {
   std::vector<ProfEv> prof_ev;
   size_t prof_used = 0;
 
-  act_t* k_of(int b) { return kv + (static_cast<size_t>(cur_slot) * blocks + b) * 2 * R_max * kHidden; }
+  act_t* k_at(int slot, int b) { return kv + (static_cast<size_t>(slot) * blocks + b) * 2 * R_max * kHidden; }
+  act_t* k_of(int b) { return k_at(cur_slot, b); }
   act_t* v_of(int b) { return k_of(b) + static_cast<size_t>(R_max) * kHidden; }
 };
 
@@ -246,8 +250,18 @@ qi_status block_gemm(qi_dit* d, qi::EpiKind kind, const act_t* a16, int R, int K
   return QI_OK;
 }
 
+// The second prompt of a two-prompt (guidance) image-only pass: its image rows
+// follow the first prompt's from row `split`; its text K/V sit in slot 1.
+struct SecondPrompt {
+  int split = 0;  // 0: a single-prompt pass
+  int L = 0;
+  const float* img_cos = nullptr;
+  const float* img_sin = nullptr;
+};
+
 qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int Lk, const float* txt_cos,
-                    const float* txt_sin, const float* img_cos, const float* img_sin, cudaStream_t s) {
+                    const float* txt_sin, const float* img_cos, const float* img_sin, cudaStream_t s,
+                    const SecondPrompt& two = SecondPrompt{}) {
   qi_dit::Block& B = d->blk[b];
   qi_dit::BlockMx* BM = d->mx_on ? &d->bmx[b] : nullptr;
   CUtensorMap m_xa, m_o, m_h;
@@ -276,6 +290,16 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
     g.txt_sin = txt_sin;
     g.img_cos = img_cos;
     g.img_sin = img_sin;
+    if (two.split > 0) {
+      g.k = d->k_at(0, b);
+      g.v = g.k + static_cast<size_t>(d->R_max) * kHidden;
+      g.split_row = two.split;
+      g.img_cos2 = two.img_cos;
+      g.img_sin2 = two.img_sin;
+      g.k2 = d->k_at(1, b);
+      g.v2 = g.k2 + static_cast<size_t>(d->R_max) * kHidden;
+      g.kv_row_off2 = two.L;
+    }
     QI_TRY(block_gemm(d, qi::kEpiQkv, d->xa, R, kHidden, m_xa, B.m_qkv, BM ? BM->m_qkv : B.m_qkv,
                       BM ? BM->sqkv : nullptr, g, s));
   }
@@ -284,15 +308,28 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
     ProfScope ps(d, s, 1);
     qi::AttnParams a{};
     a.q = d->q;
-    a.k = d->k_of(b);
-    a.v = d->v_of(b);
+    a.k = two.split > 0 ? d->k_at(0, b) : d->k_of(b);
+    a.v = a.k + static_cast<size_t>(d->R_max) * kHidden;
     a.o = d->o;
-    a.Rq = R;
+    a.Rq = two.split > 0 ? two.split : R;
     a.q_off = q_off;
     a.L = L;
     a.Lk = Lk;
     a.err = d->err;
     QI_CUDA(qi::launch_attention(a, s));
+    if (two.split > 0) {
+      // the second prompt's rows attend to its own text K/V (slot 1) and image K/V
+      const size_t off = static_cast<size_t>(two.split) * kHidden;
+      a.q = d->q + off;
+      a.o = d->o + off;
+      a.k = d->k_at(1, b);
+      a.v = a.k + static_cast<size_t>(d->R_max) * kHidden;
+      a.Rq = R - two.split;
+      a.q_off = two.L;
+      a.L = two.L;
+      a.Lk = two.L + (R - two.split);
+      QI_CUDA(qi::launch_attention(a, s));
+    }
   }
   // out-projection: x += g1 * (o Wo^T); xa = fp16(x (1 + s2))
   {
@@ -416,6 +453,35 @@ qi_status pass_head(qi_dit* d, const PassRows& pr, int N, float* vel, cudaStream
   return QI_OK;
 }
 
+// Guidance, image rows only: both prompts' N image rows in one pass of 2N rows
+// (first prompt, then second) over the text K/V in slots 0 and 1. Every GEMM
+// row is computed as in a single-prompt pass, so each half equals that prompt's
+// own image-only pass bit for bit. vel2: [2N, 64].
+qi_status run_pass_two(qi_dit* d, const float* img, int N, float t, int L1, const float* ic1, const float* is1, int L2,
+                       const float* ic2, const float* is2, float* vel2, cudaStream_t s) {
+  d->cur_slot = 0;
+  const int R = 2 * N;
+  const size_t off = static_cast<size_t>(N);
+  QI_TRY(compute_mod(d, t, s));
+  {
+    ProfScope ps(d, s, 5);
+    QI_CUDA(qi::launch_img_in(img, N, d->img_w, d->img_b, d->mod, d->x, d->xa, d->ssp, s));
+    QI_CUDA(qi::launch_img_in(img, N, d->img_w, d->img_b, d->mod, d->x + off * kHidden, d->xa + off * kHidden,
+                              d->ssp + off * kSspParts, s));
+  }
+  SecondPrompt two;
+  two.split = N;
+  two.L = L2;
+  two.img_cos = ic2;
+  two.img_sin = is2;
+  for (int b = 0; b < d->blocks; ++b) QI_TRY(run_block(d, b, R, 0, L1, L1, L1 + N, nullptr, nullptr, ic1, is1, s, two));
+  {
+    ProfScope ps(d, s, 5);
+    QI_CUDA(qi::launch_head(d->x, R, d->ssp, d->out_w, d->out_b, vel2, d->err, s));
+  }
+  return QI_OK;
+}
+
 qi_status run_pass(qi_dit* d, int slot, PassMode mode, const float* img, int N, const float* txt, int L, float t,
                    const float* tc, const float* ts, const float* ic, const float* is, float* vel,
                    cudaStream_t s) {
@@ -504,6 +570,7 @@ qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out) {
   d->L_max = cfg->L_max;
   d->N_max = cfg->N_max;
   d->R_max = cfg->L_max + cfg->N_max;
+  d->act_rows = cfg->kv_slots == 2 ? std::max(d->R_max, 2 * cfg->N_max) : d->R_max;
   d->slots = cfg->kv_slots == 2 ? 2 : 1;
   d->loaded_block.assign(cfg->blocks, false);
   cudaDeviceGetAttribute(&d->num_sms, cudaDevAttrMultiProcessorCount, device);
@@ -546,7 +613,7 @@ qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out) {
   }
 
   // ---- activations and K/V store
-  const size_t R = d->R_max;
+  const size_t R = d->act_rows;
   struct ASeg {
     void** p;
     size_t bytes;
@@ -558,8 +625,8 @@ qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out) {
       {(void**)&d->txt_a, (size_t)d->L_max * kHidden * 2}, {(void**)&d->temb_e, 2 * kTdim * 4},
       {(void**)&d->temb_h, 2 * kHidden * 4}, {(void**)&d->temb, 2 * kHidden * 4},
       {(void**)&d->mod, 2 * (size_t)kMod * 4}, {(void**)&d->err, 256}, {(void**)&d->ovf, 256},
-      {(void**)&d->kv, (size_t)d->slots * cfg->blocks * 2 * R * kHidden * 2},
-      {(void**)&d->vel_pos, d->slots == 2 ? (size_t)d->N_max * kPatch * 4 : 0},
+      {(void**)&d->kv, (size_t)d->slots * cfg->blocks * 2 * d->R_max * kHidden * 2},
+      {(void**)&d->vel_pos, d->slots == 2 ? 2 * (size_t)d->N_max * kPatch * 4 : 0},
       {(void**)&d->vel_neg, d->slots == 2 ? (size_t)d->N_max * kPatch * 4 : 0},
   };
   size_t abytes = 0;
@@ -921,15 +988,23 @@ qi_status qi_dit_step_cfg(qi_dit* d, const float* img_tokens, int N, float times
     return fail(QI_ERR_INVALID_ARG, "qi_dit_step_cfg: timestep or guidance not finite");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   QI_CUDA(cudaSetDevice(d->device));
-  const PassMode mode = use_cache ? kImage : kJoint;
-  QI_TRY(run_pass(d, 0, mode, img_tokens, N, pos_feats, L_pos, timestep, pos_txt_cos, pos_txt_sin, pos_img_cos,
-                  pos_img_sin, d->vel_pos, s));
-  QI_TRY(run_pass(d, 1, mode, img_tokens, N, neg_feats, L_neg, timestep, neg_txt_cos, neg_txt_sin, neg_img_cos,
-                  neg_img_sin, d->vel_neg, s));
+  const float* vneg = d->vel_neg;
+  if (use_cache) {
+    // both prompts in one pass of 2N rows (batch 2)
+    QI_TRY(run_pass_two(d, img_tokens, N, timestep, L_pos, pos_img_cos, pos_img_sin, L_neg, neg_img_cos, neg_img_sin,
+                        d->vel_pos, s));
+    vneg = d->vel_pos + static_cast<size_t>(N) * kPatch;
+  } else {
+    // joint passes capture each prompt's text K/V in its slot
+    QI_TRY(run_pass(d, 0, kJoint, img_tokens, N, pos_feats, L_pos, timestep, pos_txt_cos, pos_txt_sin, pos_img_cos,
+                    pos_img_sin, d->vel_pos, s));
+    QI_TRY(run_pass(d, 1, kJoint, img_tokens, N, neg_feats, L_neg, timestep, neg_txt_cos, neg_txt_sin, neg_img_cos,
+                    neg_img_sin, d->vel_neg, s));
+  }
   d->cur_slot = 0;
   {
     ProfScope ps(d, s, 5);
-    QI_CUDA(qi::launch_cfg_combine(d->vel_pos, d->vel_neg, guidance, vel, static_cast<long long>(N) * kPatch, s));
+    QI_CUDA(qi::launch_cfg_combine(d->vel_pos, vneg, guidance, vel, static_cast<long long>(N) * kPatch, s));
   }
   if (!use_cache) {
     d->cache_L[0] = L_pos;

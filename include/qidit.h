@@ -254,8 +254,11 @@ qi_status qi_dit_step(qi_dit* dit, const float* img_tokens, int N, const float* 
  * each operation rounded on its own. Each prompt has its own tables: image
  * positions carry the prompt length in their frame coordinate.
  * flags = QI_STEP_JOINT: both passes are joint and capture their slot.
- * flags = QI_STEP_USE_CACHE: image rows only; the *_feats and *_txt_* tensors
- * may be NULL; the captures must be for L_pos and L_neg.
+ * flags = QI_STEP_USE_CACHE: image rows only, both prompts in ONE pass of 2N
+ * rows (batch 2: every GEMM runs once on both prompts' rows; attention runs per
+ * prompt over its own K/V); each half equals that prompt's own image-only pass
+ * bit for bit. The *_feats and *_txt_* tensors may be NULL; the captures must be
+ * for L_pos and L_neg.
  * Errors: STATE (handle created with kv_slots != 2, no matching capture),
  * SHAPE, INVALID_ARG, CUDA. */
 qi_status qi_dit_step_cfg(qi_dit* dit, const float* img_tokens, int N, float timestep, float guidance,

@@ -98,3 +98,36 @@ def test_cfg_requires_two_slots(qi):
         assert e.value.status == 3
     finally:
         d.close()
+
+
+def test_cfg_cached_is_one_batch2_pass_bit_exact(qi):
+    """Cached guidance steps run both prompts' image rows in one pass of 2N rows. With
+    N = 400 the second prompt starts inside a 128-row GEMM tile; each half must still
+    equal that prompt's own image-only pass bit for bit, and the result the combine of
+    the two."""
+    import torch
+    h = w = 20
+    n = h * w
+    Wt = synth.Weights(seed=1, nblocks=BLOCKS)
+    d = qi.DiT(blocks=BLOCKS, L_max=max(L_POS, L_NEG), N_max=n, kv_slots=2)
+    try:
+        load_weights(d, Wt)
+        prompts = {}
+        for name, L, j in (("pos", L_POS, synth.J_TXT), ("neg", L_NEG, synth.J_TXT_LONG)):
+            tabs = orope.token_tables(L, h, w)
+            prompts[name] = dict(feats=f32_tensor(synth.input_f32(1, j, (L, 4096))), L=L,
+                                 txt_cos=f32_tensor(tabs[0]), txt_sin=f32_tensor(tabs[1]),
+                                 img_cos=f32_tensor(tabs[2]), img_sin=f32_tensor(tabs[3]))
+        x = f32_tensor(synth.input_f32(1, 61, (n, 64)))
+        d.step_cfg(x, 0.9, 3.0, prompts["pos"], prompts["neg"])                    # captures both
+        guided = d.step_cfg(x, 0.6, 3.0, prompts["pos"], prompts["neg"], use_cache=True).cpu().numpy()
+        single = {}
+        for name in ("pos", "neg"):
+            p = prompts[name]
+            single[name] = d.step(x, p["feats"], 0.6, p["txt_cos"], p["txt_sin"], p["img_cos"],
+                                  p["img_sin"]).cpu().numpy()
+        d.check()
+        assert guided.tobytes() == osched.cfg_combine(single["pos"], single["neg"], 3.0).tobytes()
+        assert torch.isfinite(torch.from_numpy(guided)).all()
+    finally:
+        d.close()
