@@ -27,6 +27,12 @@
 // Every GEMM row is computed the same way whatever M is (no split-K, fixed
 // K order), so a row's result does not depend on the other rows in the pass:
 // this is what makes the text K/V of a joint pass equal a text-only pass.
+//
+// Last wave: when the tiles left after the full waves fill at most half the
+// grid, each of them runs as two 128-column halves on two CTAs (the MMA with
+// N = 128 produces the same bits per element as with N = 256), so the last
+// wave takes half as long. Not for the gate/up GEMM, whose 256-column tiles
+// pair gate and up columns.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -51,9 +57,6 @@ struct Geo {
 };
 // MXFP8: a tile's stage-s scales sit at columns 16 s (A: +0..3, B: +4..11) of the OTHER
 // accumulator, i.e. inside the tile the epilogue is draining.
-// fp16 operands for the DiT epilogues, bf16 for the plain fp32 test hook
-template <int KIND>
-constexpr uint32_t kIdesc = KIND == kEpiF32 ? idesc_bf16_f32(kBM, kBN) : idesc_f16_f32(kBM, kBN);
 constexpr uint32_t kTmemCols = 512;  // two 256-column accumulators
 constexpr int kGroupN = 8;           // tiles sweep 8 column tiles per row tile for L2 reuse
 
@@ -65,6 +68,24 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mt
   const int local = t - g * group;
   mt = local / gsz;
   nt = first_n + local % gsz;
+}
+
+// Work unit u: a whole tile for u < tail_start, else half h of tile
+// tail_start + (u - tail_start) / 2 (columns 128 h .. 128 h + 127).
+__device__ __forceinline__ void unit_tile(int u, int tail_start, int& tile, int& half) {
+  if (u < tail_start) {
+    tile = u;
+    half = -1;
+  } else {
+    tile = tail_start + ((u - tail_start) >> 1);
+    half = (u - tail_start) & 1;
+  }
+}
+
+template <int KIND, bool MX>
+__device__ __forceinline__ uint32_t idesc_for(int n, uint32_t k) {
+  if (MX) return idesc_mxf8_f32(kBM, n, k);
+  return KIND == kEpiF32 ? idesc_bf16_f32(kBM, n) : idesc_f16_f32(kBM, n);
 }
 
 __device__ __forceinline__ float row_rinv(const float* ssp, int row) {
@@ -106,7 +127,8 @@ __device__ __forceinline__ void release_sf_cols(uint64_t* sf_bar, int c) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(sf_bar);
 }
 
-__device__ __forceinline__ void epi_qkv(const GemmParams& p, uint32_t taddr, int row, int n0, uint64_t* sf_bar) {
+__device__ __forceinline__ void epi_qkv(const GemmParams& p, uint32_t taddr, int row, int n0, int ncols,
+                                        uint64_t* sf_bar) {
   const bool valid = row < p.M;
   float rinv = 0.f;
   const float* cs = nullptr;
@@ -130,7 +152,7 @@ __device__ __forceinline__ void epi_qkv(const GemmParams& p, uint32_t taddr, int
       dst = (section == 1 ? p.k : p.v) + static_cast<size_t>(row + p.kv_row_off) * kHidden + col_in;
   }
 #pragma unroll 1
-  for (int c = 0; c < kBN / 32; ++c) {
+  for (int c = 0; c < ncols / 32; ++c) {
     uint32_t r[32];
     tmem_ld32(taddr + c * 32, r);
     tmem_ld_wait();
@@ -166,15 +188,15 @@ __device__ __forceinline__ void epi_qkv(const GemmParams& p, uint32_t taddr, int
 // ways) so that lane i handles column i of the warp's 32 rows and every global
 // access of the fp32 residual and the fp16 copy is one contiguous row segment.
 // Per row: x = acc + bias (set) or x += gate * acc; xa = fp16(x * (1 + scale));
-// the row's sum of squares over the tile's 256 columns is accumulated per lane
-// and reduced per row in a fixed order.
-__device__ __forceinline__ void epi_resid(const GemmParams& p, uint32_t taddr, int row0, int lane, int n0,
+// the row's sum of squares over each 128 columns is accumulated per lane and
+// reduced per row in a fixed order.
+__device__ __forceinline__ void epi_resid(const GemmParams& p, uint32_t taddr, int row0, int lane, int n0, int ncols,
                                           float* sm, uint64_t* sf_bar) {
   float sq[32];
 #pragma unroll
   for (int rr = 0; rr < 32; ++rr) sq[rr] = 0.f;
 #pragma unroll 1
-  for (int c = 0; c < kBN / 32; ++c) {
+  for (int c = 0; c < ncols / 32; ++c) {
     uint32_t r[32];
     tmem_ld32(taddr + c * 32, r);
     tmem_ld_wait();
@@ -211,15 +233,20 @@ __device__ __forceinline__ void epi_resid(const GemmParams& p, uint32_t taddr, i
         p.xa[idx] = __float2half_rn(xn * (txt ? s_txt : s_img));
       }
     }
+    if ((c & 3) == 3) {
+      // end of a 128-column partial: per-row sums through shared memory, fixed order
+#pragma unroll
+      for (int rr = 0; rr < 32; ++rr) sm[rr * 33 + lane] = sq[rr];
+      __syncwarp();
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) ss += sm[lane * 33 + k];
+      __syncwarp();
+      if (row0 + lane < p.M) p.ssp_out[static_cast<size_t>(row0 + lane) * kSspParts + n0 / kSspCols + c / 4] = ss;
+#pragma unroll
+      for (int rr = 0; rr < 32; ++rr) sq[rr] = 0.f;
+    }
   }
-#pragma unroll
-  for (int rr = 0; rr < 32; ++rr) sm[rr * 33 + lane] = sq[rr];
-  __syncwarp();
-  float ss = 0.f;
-#pragma unroll
-  for (int k = 0; k < 32; ++k) ss += sm[lane * 33 + k];
-  __syncwarp();
-  if (row0 + lane < p.M) p.ssp_out[static_cast<size_t>(row0 + lane) * kSspParts + n0 / kBN] = ss;
 }
 
 __device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, int row, int n0,
@@ -247,11 +274,12 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, 
   }
 }
 
-__device__ __forceinline__ void epi_f32(const GemmParams& p, uint32_t taddr, int row, int n0, uint64_t* sf_bar) {
+__device__ __forceinline__ void epi_f32(const GemmParams& p, uint32_t taddr, int row, int n0, int ncols,
+                                        uint64_t* sf_bar) {
   const bool valid = row < p.M;
   float* dst = p.d + static_cast<size_t>(row) * p.N + n0;
 #pragma unroll 1
-  for (int c = 0; c < kBN / 32; ++c) {
+  for (int c = 0; c < ncols / 32; ++c) {
     uint32_t r[32];
     tmem_ld32(taddr + c * 32, r);
     tmem_ld_wait();
@@ -290,7 +318,8 @@ __global__ void __launch_bounds__(192, 1)
   const int lane = threadIdx.x & 31;
   const int num_m = (p.M + kBM - 1) / kBM;
   const int num_n = p.N / kBN;
-  const int total = num_m * num_n;
+  const int tiles = num_m * num_n;
+  const int total = p.tail_start + 2 * (tiles - p.tail_start);  // work units
   const int kblocks = p.K / G::kK;
 
   if (threadIdx.x == 0) {
@@ -328,8 +357,12 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
         if (*abort_flag) break;
-        int mt, nt;
-        tile_coords(t, num_m, num_n, mt, nt);
+        int tile, half, mt, nt;
+        unit_tile(t, p.tail_start, tile, half);
+        tile_coords(tile, num_m, num_n, mt, nt);
+        // a half tile still loads a 256-row B box (rows past N read as zero) and uses its first 128 rows
+        const int n_row = nt * kBN + (half > 0 ? kBN / 2 : 0);
+        const int sfb_chunks = half >= 0 ? 1 : 2;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u)) {
             report_error(p.err, kErrTimeoutProducer);
@@ -337,14 +370,14 @@ __global__ void __launch_bounds__(192, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], G::kStage);
+          mbar_arrive_expect_tx(&full[stage], G::kStage - (MX ? (2 - sfb_chunks) * kSfChunk : 0));
           tma_load_2d(sA + stage * kABytes, &tmA, &full[stage], kb * G::kK, mt * kBM);
-          tma_load_2d(sB + stage * kBBytes, &tmB, &full[stage], kb * G::kK, nt * kBN);
+          tma_load_2d(sB + stage * kBBytes, &tmB, &full[stage], kb * G::kK, n_row);
           if (MX) {
             uint8_t* sf = sSF + stage * G::kSF;
             bulk_load(sf, p.sfa + (static_cast<size_t>(kb) * num_m + mt) * kSfChunk, kSfChunk, &full[stage]);
-            bulk_load(sf + kSfChunk, p.sfb + (static_cast<size_t>(kb) * (p.N / 128) + 2 * nt) * kSfChunk,
-                      2 * kSfChunk, &full[stage]);
+            bulk_load(sf + kSfChunk, p.sfb + (static_cast<size_t>(kb) * (p.N / 128) + n_row / 128) * kSfChunk,
+                      sfb_chunks * kSfChunk, &full[stage]);
           }
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -384,6 +417,9 @@ __global__ void __launch_bounds__(192, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * kBN;
+        int tile_u, half_u;
+        unit_tile(t, p.tail_start, tile_u, half_u);
+        const int n_mma = half_u >= 0 ? kBN / 2 : kBN;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&full[stage], phase)) {
             report_error(p.err, kErrTimeoutMma);
@@ -401,15 +437,15 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t sf_s = smem_u32(sSF + stage * G::kSF);
             tmem_cp_sf(sf_t, plain_rows16_desc(sf_s));
             tmem_cp_sf(sf_t + 4, plain_rows16_desc(sf_s + kSfChunk));
-            tmem_cp_sf(sf_t + 8, plain_rows16_desc(sf_s + 2 * kSfChunk));
+            if (half_u < 0) tmem_cp_sf(sf_t + 8, plain_rows16_desc(sf_s + 2 * kSfChunk));
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               mma_mxf8(d, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k),
-                       idesc_mxf8_f32(kBM, kBN, static_cast<uint32_t>(k)), sf_t, sf_t + 4, (kb | k) != 0 ? 1u : 0u);
+                       idesc_for<KIND, MX>(n_mma, static_cast<uint32_t>(k)), sf_t, sf_t + 4, (kb | k) != 0 ? 1u : 0u);
           } else {
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
-              mma_ss(d, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k), kIdesc<KIND>,
+              mma_ss(d, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k), idesc_for<KIND, MX>(n_mma, 0),
                      (kb | k) != 0 ? 1u : 0u);
           }
           mma_commit(&empty[stage]);
@@ -436,8 +472,11 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t acc = 0, acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      int mt, nt;
-      tile_coords(t, num_m, num_n, mt, nt);
+      int tile, half, mt, nt;
+      unit_tile(t, p.tail_start, tile, half);
+      tile_coords(tile, num_m, num_n, mt, nt);
+      const int n0 = nt * kBN + (half > 0 ? kBN / 2 : 0);
+      const int ncols = half >= 0 ? kBN / 2 : kBN;
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase));
       if (!ok) {
         if (lane == 0) report_error(p.err, kErrTimeoutEpilogue);
@@ -449,14 +488,14 @@ __global__ void __launch_bounds__(192, 1)
       const int row = mt * kBM + row_in_tile;
       uint64_t* sf_bar = MX ? &sffree[acc] : nullptr;
       if (KIND == kEpiQkv)
-        epi_qkv(p, taddr, row, nt * kBN, sf_bar);
+        epi_qkv(p, taddr, row, n0, ncols, sf_bar);
       else if (KIND == kEpiResid)
-        epi_resid(p, taddr, mt * kBM + quarter * 32, lane, nt * kBN,
+        epi_resid(p, taddr, mt * kBM + quarter * 32, lane, n0, ncols,
                   reinterpret_cast<float*>(smem + kStages * G::kStage + 256) + (warp - 2) * 32 * 33, sf_bar);
       else if (KIND == kEpiSwiglu)
-        epi_swiglu(p, taddr, row, nt * kBN, sf_bar);
+        epi_swiglu(p, taddr, row, nt * kBN, sf_bar);  // never split: a tile pairs gate and up columns
       else
-        epi_f32(p, taddr, row, nt * kBN, sf_bar);
+        epi_f32(p, taddr, row, n0, ncols, sf_bar);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -495,16 +534,22 @@ cudaError_t launch_any(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b,
   if (p.N % kBN != 0 || p.K % Geo<MX>::kK != 0) return cudaErrorInvalidValue;
   if (MX && (p.sfa == nullptr || p.sfb == nullptr)) return cudaErrorInvalidValue;
   const int tiles = ((p.M + kBM - 1) / kBM) * (p.N / kBN);
-  const int grid = tiles < grid_ctas ? tiles : grid_ctas;
+  // split the last wave's tiles into 128-column halves when they fill at most half the grid
+  GemmParams q = p;
+  q.tail_start = tiles;
+  const int rem = tiles % grid_ctas;
+  if (kind != kEpiSwiglu && rem > 0 && 2 * rem <= grid_ctas) q.tail_start = tiles - rem;
+  const int units = q.tail_start + 2 * (tiles - q.tail_start);
+  const int grid = units < grid_ctas ? units : grid_ctas;
   switch (kind) {
     case kEpiQkv:
-      return launch_kind<kEpiQkv, MX>(a, b, p, grid, stream);
+      return launch_kind<kEpiQkv, MX>(a, b, q, grid, stream);
     case kEpiResid:
-      return launch_kind<kEpiResid, MX>(a, b, p, grid, stream);
+      return launch_kind<kEpiResid, MX>(a, b, q, grid, stream);
     case kEpiSwiglu:
-      return launch_kind<kEpiSwiglu, MX>(a, b, p, grid, stream);
+      return launch_kind<kEpiSwiglu, MX>(a, b, q, grid, stream);
     case kEpiF32:
-      return launch_kind<kEpiF32, MX>(a, b, p, grid, stream);
+      return launch_kind<kEpiF32, MX>(a, b, q, grid, stream);
   }
   return cudaErrorInvalidValue;
 }

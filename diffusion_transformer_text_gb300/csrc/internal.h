@@ -37,11 +37,13 @@ using act_t = __half;
 
 // GEMM tile: 128 rows x 256 columns per CTA, K in steps of 64 (one 128-byte
 // swizzle span of 16-bit elements). Sum-of-squares partials are kept per
-// 256-column tile.
+// 128 columns, so that a tile split into two 128-column halves (the last
+// wave of some GEMMs) writes its own partials; consumers add them in index order.
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
-constexpr int kSspParts = kHidden / kBN;  // 16 partial sums per row
+constexpr int kSspCols = 128;                   // columns per sum-of-squares partial
+constexpr int kSspParts = kHidden / kSspCols;  // 32 partial sums per row
 
 enum EpiKind : int {
   kEpiQkv = 0,     // row scale 1/rms, RoPE on Q and K, fp16 Q / K / V stores
@@ -88,6 +90,8 @@ struct GemmParams {
   // MXFP8 variant: scale chunks of A (ceil(M/128) row groups) and B (N/128 groups)
   const uint8_t* sfa;
   const uint8_t* sfb;
+  // set by the launcher: tiles from this index on run as two 128-column halves
+  int tail_start;
 };
 
 // Launch one persistent tcgen05 GEMM D[M,N] = A[M,K] * B[N,K]^T with the

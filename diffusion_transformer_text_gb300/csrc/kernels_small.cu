@@ -142,10 +142,10 @@ __global__ void __launch_bounds__(256) block_prep_kernel(const float* __restrict
   uint4* dst = reinterpret_cast<uint4*>(xa + static_cast<size_t>(row) * kHidden + c0);
   dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
   dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-  // 16 threads cover one 256-column group
+  // 8 threads (16 columns each) cover one 128-column partial
 #pragma unroll
-  for (int o = 1; o < 16; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if ((threadIdx.x & 15) == 0) ssp[static_cast<size_t>(row) * kSspParts + threadIdx.x / 16] = ss;
+  for (int o = 1; o < 8; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 7) == 0) ssp[static_cast<size_t>(row) * kSspParts + threadIdx.x / 8] = ss;
 }
 
 // ---------------------------------------------------------------- image projection
@@ -196,11 +196,13 @@ __global__ void __launch_bounds__(256) img_in_kernel(const float* __restrict__ i
     if (lane == 0) red[r][warp] = s;
   }
   __syncthreads();
-  if (threadIdx.x < nrows) {
+  if (threadIdx.x < 2 * nrows) {
+    // two partials per row: warps 0-3 cover this block's first 128 columns, 4-7 the rest
+    const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
     float s = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) s += red[threadIdx.x][i];
-    ssp[static_cast<size_t>(r0 + threadIdx.x) * kSspParts + blockIdx.x] = s;
+    for (int i = 0; i < 4; ++i) s += red[r][4 * half + i];
+    ssp[static_cast<size_t>(r0 + r) * kSspParts + 2 * blockIdx.x + half] = s;
   }
 }
 
@@ -525,8 +527,8 @@ __global__ void __launch_bounds__(256) fbc_apply_kernel(float* __restrict__ x, c
     ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
 #pragma unroll
-  for (int o = 1; o < 16; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if ((threadIdx.x & 15) == 0) ssp[row * kSspParts + threadIdx.x / 16] = ss;
+  for (int o = 1; o < 8; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 7) == 0) ssp[row * kSspParts + threadIdx.x / 8] = ss;
 }
 
 // Full pass: rest = x_last - x1 (the residual of blocks 1..last).
