@@ -40,7 +40,7 @@ SYMBOLS = (
     "qi_dit_block_forward", "qi_dit_read_kv", "qi_dit_set_trace", "qi_dit_profile",
     "qi_dit_profile_read", "qi_last_error", "qi_gemm_bf16", "qi_attention_f16", "qi_gemm_bf16_noalloc",
     "qi_dit_step_cfg", "qi_dpmpp2m_coeffs", "qi_dpmpp2m_update", "qi_dit_step_fbcache", "qi_dit_fbcache_reset",
-    "qi_dit_set_mxfp8", "qi_quant_mxfp8", "qi_gemm_mxfp8",
+    "qi_dit_set_mxfp8", "qi_quant_mxfp8", "qi_gemm_mxfp8", "qi_debug_inject",
 )
 
 
@@ -112,6 +112,7 @@ def lib() -> ctypes.CDLL:
         "qi_dit_step_fbcache": [P, P, I, P, I, F, P, P, P, P, F, P, P, P, U, P],
         "qi_dit_fbcache_reset": [P],
         "qi_dit_set_mxfp8": [P, I],
+        "qi_debug_inject": [P, I, I],
         "qi_quant_mxfp8": [P, I, I, I, P, P, P],
         "qi_gemm_mxfp8": [P, P, P, P, P, P, I, I, I, P],
         "qi_dpmpp2m_update": [P, P, P, I, P, I, I, P],
@@ -236,6 +237,12 @@ def dpmpp2m_update(x, vel, d_prev, sigmas, i: int):
     s, sp = _host_sigmas(sigmas)
     _check(lib().qi_dpmpp2m_update(_ptr(x), _ptr(vel), _ptr(d_prev), N, sp, len(s) - 1, i, _stream()))
     return x
+
+
+def debug_inject(kind: int, arg: int = 0, dit=None):
+    """Test hook: 1 = fail the arg-th next device allocation; 2 = stall the next block GEMM
+    of `dit` until its bounded wait expires; 0 = cancel."""
+    _check(lib().qi_debug_inject(dit._h if dit is not None else None, kind, arg))
 
 
 def quant_mxfp8(x, bf16: bool):

@@ -311,7 +311,8 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint64_t* sffree = drain + 1;  // MXFP8: scale columns of accumulator a readable again
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sffree + 2);
+  uint64_t* never = sffree + 2;  // test hook: nothing ever arrives here
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -333,6 +334,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&sffree[a], 4);
     }
     mbar_init(drain, 1);
+    mbar_init(never, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -397,6 +399,11 @@ __global__ void __launch_bounds__(192, 1)
       // ---------------- MMA issuer
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
+      if (p.stall_test && !mbar_wait(never, 0)) {
+        report_error(p.err, kErrTimeoutMma);
+        *abort_flag = 1;
+        ok = false;
+      }
       int local = 0;  // tiles this CTA has issued
       for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++local) {
         if (*abort_flag) break;

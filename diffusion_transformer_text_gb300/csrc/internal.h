@@ -92,6 +92,9 @@ struct GemmParams {
   const uint8_t* sfb;
   // set by the launcher: tiles from this index on run as two 128-column halves
   int tail_start;
+  // test hook: the MMA issuer first waits on a barrier nothing arrives on, so its
+  // bounded wait expires (the launch reports kErrTimeoutMma and winds down)
+  int stall_test;
 };
 
 // Launch one persistent tcgen05 GEMM D[M,N] = A[M,K] * B[N,K]^T with the

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -88,6 +89,33 @@ qi_status make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Test hook (qi_debug_inject kind 1): when > 0, counts down device allocations
+// and fails the one that brings it to zero.
+std::atomic<int> g_fail_alloc{0};
+
+cudaError_t dev_alloc(void** p, size_t bytes) {
+  int n = g_fail_alloc.load();
+  while (n > 0) {
+    if (g_fail_alloc.compare_exchange_weak(n, n - 1)) {
+      if (n == 1) {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+      }
+      break;
+    }
+  }
+  return cudaMalloc(p, bytes);
+}
+
+// Lazy buffers: an allocation failure is QI_ERR_OOM, any other error QI_ERR_CUDA.
+#define QI_ALLOC(ptr, bytes)                                                                          \
+  do {                                                                                              \
+    cudaError_t e_ = dev_alloc(reinterpret_cast<void**>(&(ptr)), (bytes));                            \
+    if (e_ == cudaErrorMemoryAllocation) return fail(QI_ERR_OOM, "device allocation of %zu bytes failed", \
+                                                     static_cast<size_t>(bytes));                        \
+    if (e_ != cudaSuccess) return fail(QI_ERR_CUDA, "%s", cudaGetErrorString(e_));                     \
+  } while (0)
+
 }  // namespace
 
 // ---------------------------------------------------------------- handle
@@ -165,6 +193,8 @@ struct qi_dit {
   // host-I/O staging (allocated on first use)
   float *st_img = nullptr, *st_txt = nullptr, *st_tc = nullptr, *st_ts = nullptr, *st_ic = nullptr,
         *st_is = nullptr, *st_vel = nullptr;
+
+  int inject_stall = 0;  // test hook: the next block GEMM launch stalls its MMA issuer (bounded)
 
   int trace_block[2] = {-1, -1};
   float* trace_dst[2] = {nullptr, nullptr};
@@ -274,6 +304,8 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
   p.n_text = n_text;
   p.mod = d->mod;
   p.err = d->err;
+  p.stall_test = d->inject_stall;  // one-shot: only this block's QKV GEMM carries it
+  d->inject_stall = 0;
 
   // QKV + 1/rms + RoPE -> Q and this block's K/V store
   {
@@ -302,6 +334,7 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
     }
     QI_TRY(block_gemm(d, qi::kEpiQkv, d->xa, R, kHidden, m_xa, B.m_qkv, BM ? BM->m_qkv : B.m_qkv,
                       BM ? BM->sqkv : nullptr, g, s));
+    p.stall_test = 0;
   }
   // block-causal attention
   {
@@ -599,7 +632,7 @@ qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out) {
   }
   size_t wbytes = 0;
   for (auto& s : segs) wbytes += align_up(s.n * 2, A);
-  cudaError_t e = cudaMalloc(&d->wmem, wbytes);
+  cudaError_t e = dev_alloc(&d->wmem, wbytes);
   if (e != cudaSuccess) {
     delete d;
     return fail(QI_ERR_OOM, "qi_dit_create: weight store of %zu bytes: %s", wbytes, cudaGetErrorString(e));
@@ -631,7 +664,7 @@ qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out) {
   };
   size_t abytes = 0;
   for (auto& s : asegs) abytes += align_up(s.bytes, 1024);
-  e = cudaMalloc(&d->amem, abytes);
+  e = dev_alloc(&d->amem, abytes);
   if (e != cudaSuccess) {
     cudaFree(d->wmem);
     delete d;
@@ -655,7 +688,7 @@ qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out) {
                              align_up(sf_bytes(kHidden, kHidden), 1024) +
                              align_up(sf_bytes(2 * kFfn, kHidden), 1024) + align_up(sf_bytes(kHidden, kFfn), 1024);
     const size_t act = align_up(R * kFfn, 1024) + align_up(sf_bytes(R, kFfn), 1024);
-    e = cudaMalloc(&d->mxmem, per_block * cfg->blocks + act);
+    e = dev_alloc(&d->mxmem, per_block * cfg->blocks + act);
     if (e != cudaSuccess) {
       cudaFree(d->amem);
       cudaFree(d->wmem);
@@ -935,13 +968,13 @@ qi_status qi_dit_step(qi_dit* d, const float* img_tokens, int N, const float* tx
 
   if (host_io) {
     if (!d->st_img) {
-      QI_CUDA(cudaMalloc(&d->st_img, (size_t)d->N_max * kPatch * 4));
-      QI_CUDA(cudaMalloc(&d->st_vel, (size_t)d->N_max * kPatch * 4));
-      QI_CUDA(cudaMalloc(&d->st_ic, (size_t)d->N_max * kRopeCols * 4));
-      QI_CUDA(cudaMalloc(&d->st_is, (size_t)d->N_max * kRopeCols * 4));
-      QI_CUDA(cudaMalloc(&d->st_txt, (size_t)d->L_max * kHidden * 4));
-      QI_CUDA(cudaMalloc(&d->st_tc, (size_t)d->L_max * kRopeCols * 4));
-      QI_CUDA(cudaMalloc(&d->st_ts, (size_t)d->L_max * kRopeCols * 4));
+      QI_ALLOC(d->st_img, (size_t)d->N_max * kPatch * 4);
+      QI_ALLOC(d->st_vel, (size_t)d->N_max * kPatch * 4);
+      QI_ALLOC(d->st_ic, (size_t)d->N_max * kRopeCols * 4);
+      QI_ALLOC(d->st_is, (size_t)d->N_max * kRopeCols * 4);
+      QI_ALLOC(d->st_txt, (size_t)d->L_max * kHidden * 4);
+      QI_ALLOC(d->st_tc, (size_t)d->L_max * kRopeCols * 4);
+      QI_ALLOC(d->st_ts, (size_t)d->L_max * kRopeCols * 4);
     }
     const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
     QI_CUDA(cudaMemcpyAsync(d->st_img, img_tokens, (size_t)N * kPatch * 4, h2d, s));
@@ -1036,13 +1069,13 @@ qi_status qi_dit_step_fbcache(qi_dit* d, const float* img_tokens, int N, const f
   const size_t img_bytes = static_cast<size_t>(d->N_max) * kHidden * sizeof(float);
   const int grid = 4 * d->num_sms;
   if (!d->fbc_x0) {
-    QI_CUDA(cudaMalloc(&d->fbc_x0, img_bytes));
-    QI_CUDA(cudaMalloc(&d->fbc_x1, img_bytes));
-    QI_CUDA(cudaMalloc(&d->fbc_r0[0], img_bytes));
-    QI_CUDA(cudaMalloc(&d->fbc_r0[1], img_bytes));
-    QI_CUDA(cudaMalloc(&d->fbc_rest, img_bytes));
-    QI_CUDA(cudaMalloc(&d->fbc_part, static_cast<size_t>(grid) * sizeof(double2)));
-    QI_CUDA(cudaMalloc(&d->fbc_out, 2 * sizeof(double)));
+    QI_ALLOC(d->fbc_x0, img_bytes);
+    QI_ALLOC(d->fbc_x1, img_bytes);
+    QI_ALLOC(d->fbc_r0[0], img_bytes);
+    QI_ALLOC(d->fbc_r0[1], img_bytes);
+    QI_ALLOC(d->fbc_rest, img_bytes);
+    QI_ALLOC(d->fbc_part, static_cast<size_t>(grid) * sizeof(double2));
+    QI_ALLOC(d->fbc_out, 2 * sizeof(double));
   }
   d->cur_slot = 0;
   const PassMode mode = use_cache ? kImage : kJoint;
@@ -1165,6 +1198,24 @@ qi_status qi_gemm_bf16(qi_dit* d, const uint16_t* A, const uint16_t* B, float* D
   QI_CUDA(cudaSetDevice(d->device));
   QI_CUDA(qi::launch_gemm(qi::kEpiF32, ma, mb, g, d->num_sms, reinterpret_cast<cudaStream_t>(stream)));
   return QI_OK;
+}
+
+qi_status qi_debug_inject(qi_dit* d, int kind, int arg) {
+  switch (kind) {
+    case 0:
+      g_fail_alloc.store(0);
+      if (d) d->inject_stall = 0;
+      return QI_OK;
+    case 1:
+      if (arg < 1) return fail(QI_ERR_INVALID_ARG, "qi_debug_inject: allocation index %d (>= 1)", arg);
+      g_fail_alloc.store(arg);
+      return QI_OK;
+    case 2:
+      if (!d) return fail(QI_ERR_INVALID_ARG, "qi_debug_inject: kind 2 needs a handle");
+      d->inject_stall = 1;
+      return QI_OK;
+  }
+  return fail(QI_ERR_INVALID_ARG, "qi_debug_inject: kind %d", kind);
 }
 
 qi_status qi_dit_set_mxfp8(qi_dit* d, int on) {

@@ -334,6 +334,22 @@ qi_status qi_dit_read_kv(qi_dit* dit, int block, int row0, int rows, uint16_t* k
 qi_status qi_gemm_bf16(qi_dit* dit, const uint16_t* A, const uint16_t* B, float* D, int M, int N, int K,
                        qi_stream_t stream);
 
+/* Failure injection for tests [failure detection: every device wait is bounded].
+ * The pages have no counterpart; it lets a test see the library's error paths
+ * without faulting, trapping or hanging the GPU.
+ * kind 1: the arg-th next device allocation made by the library (process-wide,
+ *   dit may be NULL) fails as if the device were out of memory: the call that
+ *   makes it returns QI_ERR_OOM and frees what it had allocated.
+ * kind 2: the next block GEMM launched for `dit` first waits on a barrier that
+ *   nothing arrives on; after the 2 s limit the launch records a timeout in the
+ *   device error word and winds down (its copies drained, tensor memory freed).
+ *   The pass's result is then undefined; qi_dit_check (or the next call that
+ *   synchronises) returns QI_ERR_DEVICE_TIMEOUT and clears the word, and later
+ *   calls run normally.
+ * kind 0: cancel pending injections (of `dit`, if given).
+ * Errors: INVALID_ARG (unknown kind, arg < 1 for kind 1, NULL dit for kind 2). */
+qi_status qi_debug_inject(qi_dit* dit, int kind, int arg);
+
 /* ------------------------------------------------------------------ MXFP8 */
 
 /* Block-scaled low-precision GEMMs [MLX page: 4-bit quantised weights, an int8

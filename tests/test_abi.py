@@ -131,3 +131,11 @@ def test_dpmpp2m_coeffs_custom_schedule_and_errors(qi):
     with pytest.raises(qi.QiError) as e:
         qi.dpmpp2m_coeffs(np.array([1.5, 0.7, 0.0], np.float32), 1)   # sigma above 1
     assert e.value.status == 1
+
+
+def test_debug_inject_arguments(qi):
+    L = qi.lib()
+    assert L.qi_debug_inject(None, 9, 0) == 1           # unknown kind
+    assert L.qi_debug_inject(None, 1, 0) == 1           # allocation index must be >= 1
+    assert L.qi_debug_inject(None, 2, 0) == 1           # a stall needs a handle
+    assert L.qi_debug_inject(None, 0, 0) == 0
