@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(256) txt_prenorm_kernel(const float* __restric
 }
 
 // For a residual stream given directly: xa = fp16(x * (1 + s1[row])), plus the
-// per-256-column sums of squares. One block per row; 16 consecutive columns per thread.
+// per-128-column sums of squares. One block per row; 16 consecutive columns per thread.
 __global__ void __launch_bounds__(256) block_prep_kernel(const float* __restrict__ x, int n_text,
                                                          const float* __restrict__ mod,
                                                          act_t* __restrict__ xa, float* __restrict__ ssp) {
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(256) block_prep_kernel(const float* __restrict
 // ---------------------------------------------------------------- image projection
 
 // x[r] = img[r] . W^T + b (64 -> 4096) for image rows (sampled-t modulation),
-// xa = fp16(x * (1 + s1)), ssp = per-256-column sums of squares.
+// xa = fp16(x * (1 + s1)), ssp = per-128-column sums of squares.
 // Block: 256 columns (one per thread, its 64 weights in registers) x 64 rows.
 constexpr int kImgRows = 64;
 __global__ void __launch_bounds__(256) img_in_kernel(const float* __restrict__ img, int N,
@@ -506,7 +506,7 @@ __global__ void __launch_bounds__(kFbcThreads) fbc_finish_kernel(const double2* 
   }
 }
 
-// Skipped pass: x = x1 + rest per row, with the row's per-256-column sums of squares
+// Skipped pass: x = x1 + rest per row, with the row's per-128-column sums of squares
 // for the output head's norm. One CTA per row, 16 columns per thread.
 __global__ void __launch_bounds__(256) fbc_apply_kernel(float* __restrict__ x, const float* __restrict__ rest,
                                                         float* __restrict__ ssp) {
