@@ -171,3 +171,57 @@ def test_use_cache_requires_capture(qi):
         assert e.value.status == 3
     finally:
         d.close()
+
+
+# ---------------------------------------------------------------- degenerate and ragged shapes
+
+@pytest.mark.parametrize("L,h,w", [(1, 1, 1), (1, 1, 2), (3, 5, 3), (130, 3, 7)])
+def test_step_small_and_ragged_shapes(qi, L, h, w):
+    """One-token prompts, one-token images, non-square grids and a prompt longer than the
+    image: the two-block pass against the oracle, reuse bit-exact, capture exact."""
+    N = h * w
+    nb = 2
+    W = synth.Weights(seed=9, nblocks=nb)
+    d = qi.DiT(blocks=nb, L_max=L, N_max=N)
+    try:
+        load_weights(d, W)
+        img = synth.input_f32(9, 0, (N, 64))
+        txt = synth.input_f32(9, 1, (L, 4096))
+        tc, ts, ic, is_ = _tables(L, h, w)
+        dev = [f32_tensor(a) for a in (tc, ts, ic, is_)]
+        vel = d.step(f32_tensor(img), f32_tensor(txt), 0.7, *dev).clone()
+        cached = d.step_cached(f32_tensor(img), L, 0.7, dev[2], dev[3])
+        d.check()
+        ref = odit.dit_forward(W, img, txt, np.float32(0.7), tc, ts, ic, is_, nblocks=nb)
+        assert_close(vel.cpu().numpy(), ref, f"L={L} {h}x{w}")
+        assert np.array_equal(vel.cpu().numpy(), cached.cpu().numpy())
+        joint_kv = [t.cpu().numpy() for t in d.read_kv(1, 0, L)]
+        d.text_kv_capture(f32_tensor(txt), dev[0], dev[1])
+        d.check()
+        cap_kv = [t.cpu().numpy() for t in d.read_kv(1, 0, L)]
+        assert all(np.array_equal(a, b) for a, b in zip(joint_kv, cap_kv))
+    finally:
+        d.close()
+
+
+def test_step_rejects_out_of_range_shapes(qi):
+    d = qi.DiT(blocks=1, L_max=8, N_max=64)
+    try:
+        import torch
+        W = synth.Weights(seed=0, nblocks=1)
+        load_weights(d, W)
+        L = qi.lib()
+        z = lambda r, c: torch.zeros(r, c, device="cuda")
+        vel = z(128, 64)
+        for N, Lq in ((0, 8), (65, 8), (64, 0), (64, 9)):
+            st = L.qi_dit_step(d._h, z(max(N, 1), 64).data_ptr(), N, z(max(Lq, 1), 4096).data_ptr(), Lq, 0.5,
+                               z(max(Lq, 1), 64).data_ptr(), z(max(Lq, 1), 64).data_ptr(),
+                               z(max(N, 1), 64).data_ptr(), z(max(N, 1), 64).data_ptr(), vel.data_ptr(), 0, None)
+            assert st == 2, (N, Lq, st)
+        st = L.qi_dit_step(d._h, z(64, 64).data_ptr(), 64, z(8, 4096).data_ptr(), 8, float("nan"),
+                           z(8, 64).data_ptr(), z(8, 64).data_ptr(), z(64, 64).data_ptr(), z(64, 64).data_ptr(),
+                           vel.data_ptr(), 0, None)
+        assert st == 1
+        d.check()
+    finally:
+        d.close()
