@@ -304,7 +304,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         uint32_t r[32];
         tmem_ld32(tO + lane_off + c * 32, r);
         tmem_ld_wait();
-        if (row < p.Rq) {
+        if (row < p.Rq && p.oq) {
+          // MXFP8: these 32 O columns are one block of the out-projection's A operand
+          float ov[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __uint_as_float(r[i]) * inv;
+          const int rg = p.oq_row0 + row;
+          const int kcol = col0 + c * 32;
+          p.osf[mx_sf_offset(rg, kcol / 32, p.oq_groups)] =
+              mx_quant32(ov, p.oq + static_cast<size_t>(rg) * kHidden + kcol);
+        } else if (row < p.Rq) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {

@@ -270,7 +270,14 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, 
       const float b = __uint_as_float(u[i]) * rinv;
       hv[i] = a / (1.f + __expf(-a)) * b;
     }
-    store_f16x32(dst + c * 32, hv);
+    if (p.hq) {
+      // MXFP8: these 32 h columns are one block of the down GEMM's A operand
+      const int hcol = (n0 / kBN) * (kBN / 2) + c * 32;
+      p.hsf[mx_sf_offset(row, hcol / 32, (p.M + kBM - 1) / kBM)] =
+          mx_quant32(hv, p.hq + static_cast<size_t>(row) * kFfn + hcol);
+    } else {
+      store_f16x32(dst + c * 32, hv);
+    }
   }
 }
 

@@ -77,6 +77,8 @@ struct GemmParams {
   int kv_row_off2;
   // kEpiSwiglu
   act_t* h;
+  uint8_t* hq;   // MXFP8 (if set): h written as E4M3 codes [M][kFfn] and scales (hsf) instead of fp16
+  uint8_t* hsf;
   // kEpiResid
   float* x;                 // fp32 residual stream [M][kHidden]
   act_t* xa;                // fp16(x * (1 + scale)) for the next GEMM
@@ -129,6 +131,12 @@ struct AttnParams {
   int L;           // text rows: global index < L
   int Lk;          // keys visible to image rows
   int* err;        // device error word (may be null)
+  // MXFP8 (if oq is set): O written as E4M3 codes and scales for the out-projection
+  // instead of fp16 o; query row r is row oq_row0 + r of that A operand
+  uint8_t* oq;
+  uint8_t* osf;
+  int oq_row0;
+  int oq_groups;   // ceil(A operand rows / 128)
 };
 
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);

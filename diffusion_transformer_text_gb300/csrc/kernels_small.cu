@@ -420,26 +420,7 @@ __global__ void quant_mx_kernel(const uint16_t* __restrict__ in, int rows, int K
       }
     }
   }
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  int e = amax > 0.f ? ilogbf(amax) - 8 : -127;
-  e = max(-127, min(127, e));
-  const float inv = ldexpf(1.f, -e);  // exact power of two
-  uint32_t packed[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i] * inv, v[4 * i + 1] * inv), __NV_SATFINITE,
-                                                 __NV_E4M3);
-    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i + 2] * inv, v[4 * i + 3] * inv), __NV_SATFINITE,
-                                                 __NV_E4M3);
-    packed[i] = (lo & 0xFFFFu) | (hi << 16);
-  }
-  uint4* dst = reinterpret_cast<uint4*>(q + static_cast<size_t>(r) * K + kb * 32);
-  dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-  const size_t chunk = static_cast<size_t>(kb / 4) * groups + r / 128;
-  sf[chunk * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + (kb % 4)] = static_cast<uint8_t>(e + 127);
+  sf[mx_sf_offset(r, kb, groups)] = mx_quant32(v, q + static_cast<size_t>(r) * K + kb * 32);
 }
 
 // ---------------------------------------------------------------- first-block cache

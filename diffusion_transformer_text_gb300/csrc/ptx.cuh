@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cstdint>
 
 namespace qi {
@@ -309,6 +310,39 @@ __device__ __forceinline__ uint64_t plain_rows16_desc(uint32_t saddr) {
   d |= static_cast<uint64_t>(128 >> 4) << 32;
   d |= static_cast<uint64_t>(1) << 46;
   return d;
+}
+
+// MXFP8 block of 32 values (OCP MX v1.0): shared exponent e = floor(log2 max|v|) - 8
+// (8 = exponent of E4M3's largest normal, 448), clamped to [-127, 127], -127 for an
+// all-zero block; each value E4M3(v * 2^-e), round to nearest even, clamped to
+// +-448. Writes the 32 codes to dst (16-byte aligned) and returns the scale byte e + 127.
+__device__ __forceinline__ uint8_t mx_quant32(const float (&v)[32], uint8_t* dst) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  int e = amax > 0.f ? ilogbf(amax) - 8 : -127;
+  e = max(-127, min(127, e));
+  const float inv = ldexpf(1.f, -e);  // exact power of two
+  uint32_t packed[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i] * inv, v[4 * i + 1] * inv), __NV_SATFINITE,
+                                                 __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i + 2] * inv, v[4 * i + 3] * inv), __NV_SATFINITE,
+                                                 __NV_E4M3);
+    packed[i] = (lo & 0xFFFFu) | (hi << 16);
+  }
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  d4[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  d4[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  return static_cast<uint8_t>(e + 127);
+}
+
+// Byte offset of the scale of row r, 32-value block kb in the MXFP8 scale layout:
+// 512-byte chunks of 128 rows x 4 blocks, ordered [kb / 4][r / 128], byte
+// (r % 32) * 16 + ((r % 128) / 32) * 4 + kb % 4 inside a chunk; `groups` = ceil(rows / 128).
+__device__ __forceinline__ size_t mx_sf_offset(int r, int kb, int groups) {
+  return (static_cast<size_t>(kb / 4) * groups + r / 128) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + (kb % 4);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

@@ -18,6 +18,7 @@
 #include "../../include/qidit.h"
 #include "internal.h"
 
+using qi::kBM;
 using qi::kBN;
 using qi::kFfn;
 using qi::kHidden;
@@ -153,8 +154,10 @@ struct qi_dit {
   };
   std::vector<BlockMx> bmx;
   void* mxmem = nullptr;
-  uint8_t* aq = nullptr;   // [R_max, 12288] E4M3 activations (the GEMM's A operand)
+  uint8_t* aq = nullptr;   // [act_rows, 12288] E4M3 activations (a GEMM's A operand)
   uint8_t* asf = nullptr;  // their scale chunks
+  uint8_t* hq = nullptr;   // [act_rows, 12288] E4M3 SwiGLU output, written by the gate/up epilogue
+  uint8_t* hsf = nullptr;
 
   // activations (one allocation)
   void* amem = nullptr;
@@ -266,15 +269,20 @@ qi_status compute_mod(qi_dit* d, float t, cudaStream_t s) {
 // quantised into the handle's E4M3 buffer first and the block's MXFP8 weights.
 qi_status block_gemm(qi_dit* d, qi::EpiKind kind, const act_t* a16, int R, int K, const CUtensorMap& m_a16,
                      const CUtensorMap& m_w16, const CUtensorMap& m_w8, const uint8_t* w_sf, qi::GemmParams g,
-                     cudaStream_t s) {
+                     cudaStream_t s, const uint8_t* a8 = nullptr, const uint8_t* a8_sf = nullptr) {
   if (!d->mx_on) {
     QI_CUDA(qi::launch_gemm(kind, m_a16, m_w16, g, d->num_sms, s));
     return QI_OK;
   }
-  QI_CUDA(qi::launch_quant_mx(reinterpret_cast<const uint16_t*>(a16), false, R, K, d->aq, d->asf, s));
+  if (!a8) {
+    // quantise the fp16 operand into the handle's buffer
+    QI_CUDA(qi::launch_quant_mx(reinterpret_cast<const uint16_t*>(a16), false, R, K, d->aq, d->asf, s));
+    a8 = d->aq;
+    a8_sf = d->asf;
+  }
   CUtensorMap m_a8;
-  if (!qi::encode_map8(&m_a8, d->aq, R, K, 128)) return fail(QI_ERR_CUDA, "8-bit tensor map encoding failed");
-  g.sfa = d->asf;
+  if (!qi::encode_map8(&m_a8, a8, R, K, 128)) return fail(QI_ERR_CUDA, "8-bit tensor map encoding failed");
+  g.sfa = a8_sf;
   g.sfb = w_sf;
   QI_CUDA(qi::launch_gemm_mx(kind, m_a8, m_w8, g, d->num_sms, s));
   return QI_OK;
@@ -349,6 +357,13 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
     a.L = L;
     a.Lk = Lk;
     a.err = d->err;
+    if (d->mx_on) {
+      // O straight into the out-projection's MXFP8 A operand (no fp16 copy)
+      a.oq = d->aq;
+      a.osf = d->asf;
+      a.oq_row0 = 0;
+      a.oq_groups = (R + kBM - 1) / kBM;
+    }
     QI_CUDA(qi::launch_attention(a, s));
     if (two.split > 0) {
       // the second prompt's rows attend to its own text K/V (slot 1) and image K/V
@@ -361,6 +376,7 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
       a.q_off = two.L;
       a.L = two.L;
       a.Lk = two.L + (R - two.split);
+      a.oq_row0 = two.split;
       QI_CUDA(qi::launch_attention(a, s));
     }
   }
@@ -377,7 +393,7 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
     g.gate_chunk = 1;
     g.scale_chunk = 2;
     QI_TRY(block_gemm(d, qi::kEpiResid, d->o, R, kHidden, m_o, B.m_o, BM ? BM->m_o : B.m_o, BM ? BM->so : nullptr, g,
-                      s));
+                      s, BM ? d->aq : nullptr, BM ? d->asf : nullptr));
   }
   // gate/up + SwiGLU
   {
@@ -387,6 +403,11 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
     g.K = kHidden;
     g.ssp_in = d->ssp;
     g.h = d->h;
+    if (BM) {
+      // h straight into the down GEMM's MXFP8 A operand
+      g.hq = d->hq;
+      g.hsf = d->hsf;
+    }
     QI_TRY(block_gemm(d, qi::kEpiSwiglu, d->xa, R, kHidden, m_xa, B.m_gu, BM ? BM->m_gu : B.m_gu,
                       BM ? BM->sgu : nullptr, g, s));
   }
@@ -403,7 +424,7 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
     g.gate_chunk = 3;
     g.scale_chunk = 0;
     QI_TRY(block_gemm(d, qi::kEpiResid, d->h, R, kFfn, m_h, B.m_d, BM ? BM->m_d : B.m_d, BM ? BM->sd : nullptr, g,
-                      s));
+                      s, BM ? d->hq : nullptr, BM ? d->hsf : nullptr));
   }
   return QI_OK;
 }
@@ -687,7 +708,7 @@ qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out) {
                              align_up((size_t)kHidden * kFfn, 1024) + align_up(sf_bytes(3 * kHidden, kHidden), 1024) +
                              align_up(sf_bytes(kHidden, kHidden), 1024) +
                              align_up(sf_bytes(2 * kFfn, kHidden), 1024) + align_up(sf_bytes(kHidden, kFfn), 1024);
-    const size_t act = align_up(R * kFfn, 1024) + align_up(sf_bytes(R, kFfn), 1024);
+    const size_t act = 2 * (align_up(R * kFfn, 1024) + align_up(sf_bytes(R, kFfn), 1024));
     e = dev_alloc(&d->mxmem, per_block * cfg->blocks + act);
     if (e != cudaSuccess) {
       cudaFree(d->amem);
@@ -714,6 +735,8 @@ qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out) {
     }
     d->aq = take(R * kFfn);
     d->asf = take(sf_bytes(R, kFfn));
+    d->hq = take(R * kFfn);
+    d->hsf = take(sf_bytes(R, kFfn));
     d->has_mx = true;
   }
 
