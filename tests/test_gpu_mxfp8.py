@@ -176,3 +176,36 @@ def test_mxfp8_requires_the_weight_copy(qi):
         assert e.value.status == 3
     finally:
         d.close()
+
+
+def test_mxfp8_guidance_batch2_bit_exact(qi):
+    """MXFP8 mode with both prompts in one pass: the second prompt's attention output is
+    quantised into the out-projection operand at a row offset (N = 400 starts it inside a
+    128-row tile); each half must equal that prompt's own MXFP8 image-only pass."""
+    from oracle import sched as osched
+    h = w = 20
+    n = h * w
+    nb = 2
+    Wt = synth.Weights(seed=1, nblocks=nb)
+    d = qi.DiT(blocks=nb, L_max=22, N_max=n, kv_slots=2, mxfp8=True)
+    try:
+        load_weights(d, Wt)
+        d.set_mxfp8(True)
+        prompts = {}
+        for name, L, j in (("pos", 22, synth.J_TXT), ("neg", 9, synth.J_TXT_LONG)):
+            tabs = orope.token_tables(L, h, w)
+            prompts[name] = dict(feats=f32_tensor(synth.input_f32(1, j, (L, 4096))), L=L,
+                                 txt_cos=f32_tensor(tabs[0]), txt_sin=f32_tensor(tabs[1]),
+                                 img_cos=f32_tensor(tabs[2]), img_sin=f32_tensor(tabs[3]))
+        x = f32_tensor(synth.input_f32(1, 62, (n, 64)))
+        d.step_cfg(x, 0.9, 2.0, prompts["pos"], prompts["neg"])
+        guided = d.step_cfg(x, 0.5, 2.0, prompts["pos"], prompts["neg"], use_cache=True).cpu().numpy()
+        single = {}
+        for name in ("pos", "neg"):
+            p = prompts[name]
+            single[name] = d.step(x, p["feats"], 0.5, p["txt_cos"], p["txt_sin"], p["img_cos"],
+                                  p["img_sin"]).cpu().numpy()
+        d.check()
+        assert guided.tobytes() == osched.cfg_combine(single["pos"], single["neg"], 2.0).tobytes()
+    finally:
+        d.close()
