@@ -168,6 +168,17 @@ def cores_used() -> int:
     return os.cpu_count() or 1
 
 
+def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's figure: the replicas run at once and the job ends with the last."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
@@ -278,11 +289,7 @@ def run_ours(args, rank, world, local_rank):
     prof = dit.profile_read()
     dit.profile(False)
     dit.check()
-    ms = e0.elapsed_time(e1)
-    ms_t = torch.tensor([ms], dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms = float(ms_t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
 
     njoint = sum(1 for i in range(args.steps) if i % STEPS_PER_IMAGE == 0)
     nimg = args.steps - njoint
@@ -418,11 +425,7 @@ def run_ours(args, rank, world, local_rank):
     for i in range(e2e_steps):
         e2e_step(i)
     torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t0
-    e2e_t = torch.tensor([e2e_s], dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-    e2e_s = float(e2e_t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     h2d = (N * 64 * 4 + 2 * N * 64 * 4) * e2e_steps + njoint * (L * HIDDEN * 4 + 2 * L * 64 * 4)
     d2h = N * 64 * 4 * e2e_steps
 
