@@ -16,10 +16,17 @@
 // first 64 columns of the other accumulator: written only after the previous
 // tile's MMAs have completed and its epilogue has read those columns.
 //
+// Two kernels share the epilogues. The fp16 / bf16 GEMMs run on CTA pairs
+// (gemm_pair_tc: a cluster of two CTAs computes 256 x 256 tiles with
+// tcgen05.mma.cta_group::2, each CTA loading its 128 A rows and half of the B
+// rows); the MXFP8 GEMM runs one CTA per 128 x 256 tile (gemm_bf16_tc).
+//
 // Roles per CTA (192 threads):
-//   warp 0     TMA producer: 128x64 A and 256x64 B tiles into a 4-stage ring
-//   warp 1     TMEM owner and MMA issuer (one thread): 4 x tcgen05.mma 128x256x16
-//              per stage, accumulating into one of two 256-column TMEM buffers
+//   warp 0     TMA producer: A and B tiles into a ring of stages (pair: 128x64 A
+//              and 128x64 B, 6 stages; single: 128x64 A and 256x64 B, 4 stages)
+//   warp 1     TMEM owner and MMA issuer (one thread; the pair's leader only):
+//              4 x tcgen05.mma per stage (K = 16 each; M = 256 across the pair or
+//              128), accumulating into one of two 256-column TMEM buffers
 //   warps 2-5  epilogue: each thread owns one accumulator row (TMEM lane),
 //              reads 32 columns at a time and applies the fused epilogue while
 //              the MMA warp fills the other TMEM buffer.
@@ -29,10 +36,10 @@
 // this is what makes the text K/V of a joint pass equal a text-only pass.
 //
 // Last wave: when the tiles left after the full waves fill at most half the
-// grid, each of them runs as two 128-column halves on two CTAs (the MMA with
-// N = 128 produces the same bits per element as with N = 256), so the last
-// wave takes half as long. Not for the gate/up GEMM, whose 256-column tiles
-// pair gate and up columns.
+// grid (of CTAs, or of pairs), each of them runs as two 128-column halves (the
+// MMA with N = 128 produces the same bits per element as with N = 256), so the
+// last wave takes half as long. Not for the gate/up GEMM, whose 256-column
+// tiles pair gate and up columns.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -527,6 +534,275 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// ---------------------------------------------------------------- CTA-pair kernel
+//
+// fp16 / bf16 operands: a cluster of two CTAs computes 256 x 256 tiles with
+// tcgen05.mma.cta_group::2. Each CTA loads its own 128 A rows and half of the
+// tile's 256 B rows (16 KB + 16 KB per stage, 6 stages); both CTAs' loads count
+// on the leader's `full` barrier; the leader's single MMA thread issues
+// M = 256 MMAs and its commits arrive on the barriers of both CTAs (stage free,
+// accumulator full, drain). Each CTA's epilogue warps drain their own 128
+// accumulator rows and arrive on the leader's `tempty` barrier (4 warps x 2).
+// Per SM this halves the B bytes loaded and read by the tensor core per MMA.
+constexpr int kPairStages = 6;
+constexpr int kPairB = (kBN / 2) * kBK * 2;     // 16 KB: this CTA's half of the B tile
+constexpr int kPairStage = kABytes + kPairB;    // 32 KB
+constexpr int kPairSmem = kPairStages * kPairStage + 1024 + 256 + kEpiScratch;
+constexpr int kPairRows = 2 * kBM;              // rows of a pair tile
+
+template <int KIND>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+    gemm_pair_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  // the same offsets in both CTAs: the pair's MMA addresses the peer's operands by them
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kPairStages * kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStage);  // leader's are used
+  uint64_t* empty = full + kPairStages;
+  uint64_t* tfull = empty + kPairStages;
+  uint64_t* tempty = tfull + 2;  // leader's are used
+  uint64_t* drain = tempty + 2;
+  uint64_t* never = drain + 1;   // test hook: nothing ever arrives here
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  const int num_m = (p.M + kPairRows - 1) / kPairRows;
+  const int num_n = p.N / kBN;
+  const int tiles = num_m * num_n;
+  const int total = p.tail_start + 2 * (tiles - p.tail_start);  // work units
+  const int kblocks = p.K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);
+    }
+    mbar_init(drain, 1);
+    mbar_init(never, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs): own A rows and own half of B
+      const uint32_t full_leader = mapa_shared(smem_u32(&full[0]), 0);
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;  // leader: stages whose expect_tx it posted
+      bool ok = true;
+      for (int t = pair; ok && t < total; t += npairs) {
+        if (*abort_flag) break;
+        int tile, half, mt, nt;
+        unit_tile(t, p.tail_start, tile, half);
+        tile_coords(tile, num_m, num_n, mt, nt);
+        const int a_row = mt * kPairRows + static_cast<int>(rank) * kBM;
+        // a half tile (N = 128) takes 64 B rows from each CTA; the 128-row box's
+        // other rows are loaded but not read
+        const int b_rows = half >= 0 ? kBN / 4 : kBN / 2;
+        const int b_row = nt * kBN + (half > 0 ? kBN / 2 : 0) + static_cast<int>(rank) * b_rows;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u)) {
+            report_error(p.err, kErrTimeoutProducer);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          if (rank == 0) {
+            mbar_arrive_expect_tx(&full[stage], 2 * kPairStage);
+            issued_mask |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          }
+          tma_load_2d_pair(sA + stage * kABytes, &tmA, full_leader + 8u * stage, kb * kBK, a_row);
+          tma_load_2d_pair(sB + stage * kPairB, &tmB, full_leader + 8u * stage, kb * kBK, b_row);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // the leader's posted stages must complete (both CTAs' bytes) before the pair may exit
+      if (rank == 0)
+        for (int s = 0; s < kPairStages; ++s)
+          if ((issued_mask >> s) & 1u)
+            if (!mbar_wait(&full[s], (issued_parity >> s) & 1u)) report_error(p.err, kErrTimeoutDrain);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (leader only)
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      if (p.stall_test && !mbar_wait(never, 0)) {
+        report_error(p.err, kErrTimeoutMma);
+        *abort_flag = 1;
+        ok = false;
+      }
+      for (int t = pair; ok && t < total; t += npairs) {
+        if (*abort_flag) break;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u)) {
+          report_error(p.err, kErrTimeoutMma);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * kBN;
+        int tile_u, half_u;
+        unit_tile(t, p.tail_start, tile_u, half_u);
+        const int n_mma = half_u >= 0 ? kBN / 2 : kBN;
+        const uint32_t idesc =
+            KIND == kEpiF32 ? idesc_bf16_f32(kPairRows, n_mma) : idesc_f16_f32(kPairRows, n_mma);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase)) {
+            report_error(p.err, kErrTimeoutMma);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * kABytes);
+          const uint32_t b0 = smem_u32(sB + stage * kPairB);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_ss_pair(d, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k), idesc,
+                        (kb | k) != 0 ? 1u : 0u);
+          mma_commit_pair(&empty[stage]);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // arrives in both CTAs once every MMA above has completed
+      mma_commit_pair(drain);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5 of both CTAs): this CTA's 128 rows
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_in_tile = static_cast<int>(rank) * kBM + quarter * 32 + lane;
+    const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[0]), 0);
+    uint32_t acc = 0, acc_phase = 0;
+    for (int t = pair; t < total; t += npairs) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      int tile, half, mt, nt;
+      unit_tile(t, p.tail_start, tile, half);
+      tile_coords(tile, num_m, num_n, mt, nt);
+      const int n0 = nt * kBN + (half > 0 ? kBN / 2 : 0);
+      const int ncols = half >= 0 ? kBN / 2 : kBN;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase));
+      if (!ok) {
+        if (lane == 0) report_error(p.err, kErrTimeoutEpilogue);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN;
+      const int row = mt * kPairRows + row_in_tile;
+      if (KIND == kEpiQkv)
+        epi_qkv(p, taddr, row, n0, ncols, nullptr);
+      else if (KIND == kEpiResid)
+        epi_resid(p, taddr, row - lane, lane, n0, ncols,
+                  reinterpret_cast<float*>(smem + kPairStages * kPairStage + 256) + (warp - 2) * 32 * 33, nullptr);
+      else if (KIND == kEpiSwiglu)
+        epi_swiglu(p, taddr, row, nt * kBN, nullptr);  // never split: a tile pairs gate and up columns
+      else
+        epi_f32(p, taddr, row, n0, ncols, nullptr);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  // all MMAs done (they read both CTAs' shared memory and write both TMEMs)
+  if (warp == 1 && lane == 0 && !mbar_wait(drain, 0)) report_error(p.err, kErrTimeoutDrain);
+  __syncwarp();
+  __syncthreads();
+  if (rank != 0 && threadIdx.x == 0 && *abort_flag) {
+    // after an abort the peer's last loads may not have been consumed by the
+    // leader's MMAs; they land within microseconds (their barrier is the leader's)
+    const unsigned long long t0 = globaltimer();
+    while (globaltimer() - t0 < 200000ull) {
+    }
+  }
+  tc_fence_before();
+  cluster_sync();  // neither CTA leaves while the other may still touch its shared memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+template <int KIND>
+cudaError_t launch_pair_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
+                             cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_pair_tc<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  gemm_pair_tc<KIND><<<grid, 192, kPairSmem, stream>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pair_any(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                            int grid_ctas, cudaStream_t stream) {
+  if (p.M <= 0) return cudaSuccess;
+  if (p.N % kBN != 0 || p.K % kBK != 0) return cudaErrorInvalidValue;
+  const int clusters = grid_ctas / 2;
+  if (clusters < 1) return cudaErrorInvalidValue;
+  const int tiles = ((p.M + kPairRows - 1) / kPairRows) * (p.N / kBN);
+  // split the last wave's tiles into 128-column halves when they fill at most half the pairs
+  GemmParams q = p;
+  q.tail_start = tiles;
+  const int rem = tiles % clusters;
+  if (kind != kEpiSwiglu && rem > 0 && 2 * rem <= clusters) q.tail_start = tiles - rem;
+  const int units = q.tail_start + 2 * (tiles - q.tail_start);
+  const int grid = 2 * (units < clusters ? units : clusters);
+  switch (kind) {
+    case kEpiQkv:
+      return launch_pair_kind<kEpiQkv>(a, b, q, grid, stream);
+    case kEpiResid:
+      return launch_pair_kind<kEpiResid>(a, b, q, grid, stream);
+    case kEpiSwiglu:
+      return launch_pair_kind<kEpiSwiglu>(a, b, q, grid, stream);
+    case kEpiF32:
+      return launch_pair_kind<kEpiF32>(a, b, q, grid, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
 template <int KIND, bool MX>
 cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
                         cudaStream_t stream) {
@@ -572,7 +848,7 @@ cudaError_t launch_any(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b,
 
 cudaError_t launch_gemm(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                         int grid_ctas, cudaStream_t stream) {
-  return launch_any<false>(kind, a, b, p, grid_ctas, stream);
+  return launch_pair_any(kind, a, b, p, grid_ctas, stream);
 }
 
 cudaError_t launch_gemm_mx(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,

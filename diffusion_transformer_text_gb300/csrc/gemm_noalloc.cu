@@ -118,7 +118,7 @@ extern "C" qi_status qi_gemm_bf16_noalloc(const uint16_t* A, const uint16_t* B, 
   qi_status st = device_slot(&slot);
   if (st != QI_OK) return st;
   CUtensorMap ma, mb;
-  if (!encode_map(&ma, A, M, K, 128) || !encode_map(&mb, B, N, K, 256))
+  if (!encode_map(&ma, A, M, K, 128) || !encode_map(&mb, B, N, K, qi::kBoxRowsPair))
     return noalloc_fail(QI_ERR_CUDA, "qi_gemm_bf16_noalloc: tensor map encoding failed");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the status word must start at zero for this call

@@ -39,9 +39,13 @@ using act_t = __half;
 // swizzle span of 16-bit elements). Sum-of-squares partials are kept per
 // 128 columns, so that a tile split into two 128-column halves (the last
 // wave of some GEMMs) writes its own partials; consumers add them in index order.
+// The fp16 / bf16 GEMMs run on CTA pairs (256 x 256 per pair, 128 rows per CTA);
+// each CTA loads half of the 256 B rows, so their B tensor maps use 128-row
+// boxes (kBoxRowsPair). The MXFP8 GEMM runs one CTA per tile (256-row B boxes).
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
+constexpr int kBoxRowsPair = kBN / 2;
 constexpr int kSspCols = 128;                   // columns per sum-of-squares partial
 constexpr int kSspParts = kHidden / kSspCols;  // 32 partial sums per row
 

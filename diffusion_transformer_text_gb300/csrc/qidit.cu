@@ -740,14 +740,16 @@ qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out) {
     d->has_mx = true;
   }
 
-  // ---- weight tensor maps (B operands: 256-row boxes)
-  qi_status st = make_map(&d->m_txt, d->txt_w, kHidden, kHidden, 256);
+  // ---- weight tensor maps (B operands: 128-row boxes for the CTA-pair fp16 GEMM,
+  // 256-row boxes for the MXFP8 GEMM)
+  const uint32_t bx = qi::kBoxRowsPair;
+  qi_status st = make_map(&d->m_txt, d->txt_w, kHidden, kHidden, bx);
   for (int b = 0; st == QI_OK && b < cfg->blocks; ++b) {
     auto& B = d->blk[b];
-    st = make_map(&B.m_qkv, B.wqkv, 3 * kHidden, kHidden, 256);
-    if (st == QI_OK) st = make_map(&B.m_o, B.wo, kHidden, kHidden, 256);
-    if (st == QI_OK) st = make_map(&B.m_gu, B.wgu, 2 * kFfn, kHidden, 256);
-    if (st == QI_OK) st = make_map(&B.m_d, B.wd, kHidden, kFfn, 256);
+    st = make_map(&B.m_qkv, B.wqkv, 3 * kHidden, kHidden, bx);
+    if (st == QI_OK) st = make_map(&B.m_o, B.wo, kHidden, kHidden, bx);
+    if (st == QI_OK) st = make_map(&B.m_gu, B.wgu, 2 * kFfn, kHidden, bx);
+    if (st == QI_OK) st = make_map(&B.m_d, B.wd, kHidden, kFfn, bx);
     if (st == QI_OK && d->has_mx) {
       auto& M = d->bmx[b];
       if (!qi::encode_map8(&M.m_qkv, M.wqkv, 3 * kHidden, kHidden, 256) ||
@@ -1211,7 +1213,7 @@ qi_status qi_gemm_bf16(qi_dit* d, const uint16_t* A, const uint16_t* B, float* D
     return fail(QI_ERR_SHAPE, "qi_gemm_bf16: M %d N %d K %d", M, N, K);
   CUtensorMap ma, mb;
   QI_TRY(make_map(&ma, A, M, K, 128, true));
-  QI_TRY(make_map(&mb, B, N, K, 256, true));
+  QI_TRY(make_map(&mb, B, N, K, qi::kBoxRowsPair, true));
   qi::GemmParams g{};
   g.M = M;
   g.N = N;
