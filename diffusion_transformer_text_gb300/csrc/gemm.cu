@@ -275,7 +275,9 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, 
     for (int i = 0; i < 32; ++i) {
       const float a = __uint_as_float(g[i]) * rinv;
       const float b = __uint_as_float(u[i]) * rinv;
-      hv[i] = a / (1.f + __expf(-a)) * b;
+      // silu(a) = a / (1 + e^-a) with the fast division: its few-ulp error is far
+      // below the fp16 / E4M3 rounding of h (and e^-a = inf gives -0, the limit)
+      hv[i] = __fdividef(a, 1.f + __expf(-a)) * b;
     }
     if (p.hq) {
       // MXFP8: these 32 h columns are one block of the down GEMM's A operand
