@@ -134,6 +134,16 @@ __device__ __forceinline__ void release_sf_cols(uint64_t* sf_bar, int c) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(sf_bar);
 }
 
+// The same release right after the warp has read columns 0..63 into registers
+// (the QKV and SwiGLU epilogues read them first, so the MMA issuer can start the
+// next tile's scale copies before the rest of the epilogue runs).
+__device__ __forceinline__ void release_sf_now(uint64_t* sf_bar) {
+  tc_fence_before();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(sf_bar);
+}
+
+template <bool EARLY>
 __device__ __forceinline__ void epi_qkv(const GemmParams& p, uint32_t taddr, int row, int n0, int ncols,
                                         uint64_t* sf_bar) {
   const bool valid = row < p.M;
@@ -158,13 +168,8 @@ __device__ __forceinline__ void epi_qkv(const GemmParams& p, uint32_t taddr, int
     else
       dst = (section == 1 ? p.k : p.v) + static_cast<size_t>(row + p.kv_row_off) * kHidden + col_in;
   }
-#pragma unroll 1
-  for (int c = 0; c < ncols / 32; ++c) {
-    uint32_t r[32];
-    tmem_ld32(taddr + c * 32, r);
-    tmem_ld_wait();
-    release_sf_cols(sf_bar, c);
-    if (!valid) continue;
+  auto chunk = [&](int c, const uint32_t(&r)[32]) {
+    if (!valid) return;
     float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * rinv;
@@ -187,6 +192,26 @@ __device__ __forceinline__ void epi_qkv(const GemmParams& p, uint32_t taddr, int
       }
     }
     store_f16x32(dst + c * 32, v);
+  };
+  int c0 = 0;
+  if (EARLY) {
+    // MXFP8: columns 0..63 hold the next tile's scale sets once released
+    uint32_t r0[32], r1[32];
+    tmem_ld32(taddr, r0);
+    tmem_ld32(taddr + 32, r1);
+    tmem_ld_wait();
+    release_sf_now(sf_bar);
+    chunk(0, r0);
+    chunk(1, r1);
+    c0 = 2;
+  }
+#pragma unroll 1
+  for (int c = c0; c < ncols / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(taddr + c * 32, r);
+    tmem_ld_wait();
+    if (!EARLY) release_sf_cols(sf_bar, c);
+    chunk(c, r);
   }
 }
 
@@ -256,20 +281,15 @@ __device__ __forceinline__ void epi_resid(const GemmParams& p, uint32_t taddr, i
   }
 }
 
+template <bool EARLY>
 __device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, int row, int n0,
                                            uint64_t* sf_bar) {
   const bool valid = row < p.M;
   const float rinv = valid ? row_rinv(p.ssp_in, row) : 0.f;
   // tile columns [0,128) are gate rows 128j.., [128,256) the matching up rows
   act_t* dst = p.h + static_cast<size_t>(row) * kFfn + (n0 / kBN) * (kBN / 2);
-#pragma unroll 1
-  for (int c = 0; c < kBN / 64; ++c) {
-    uint32_t g[32], u[32];
-    tmem_ld32(taddr + c * 32, g);
-    tmem_ld32(taddr + kBN / 2 + c * 32, u);
-    tmem_ld_wait();
-    release_sf_cols(sf_bar, c);
-    if (!valid) continue;
+  auto chunk = [&](int c, const uint32_t(&g)[32], const uint32_t(&u)[32]) {
+    if (!valid) return;
     float hv[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
@@ -287,6 +307,37 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, 
     } else {
       store_f16x32(dst + c * 32, hv);
     }
+  };
+  int c0 = 0;
+  if (EARLY) {
+    // MXFP8: gate columns 0..63 hold the next tile's scale sets once released
+    uint32_t g0[32], g1[32];
+    tmem_ld32(taddr, g0);
+    tmem_ld32(taddr + 32, g1);
+    tmem_ld_wait();
+    release_sf_now(sf_bar);
+    {
+      uint32_t u[32];
+      tmem_ld32(taddr + kBN / 2, u);
+      tmem_ld_wait();
+      chunk(0, g0, u);
+    }
+    {
+      uint32_t u[32];
+      tmem_ld32(taddr + kBN / 2 + 32, u);
+      tmem_ld_wait();
+      chunk(1, g1, u);
+    }
+    c0 = 2;
+  }
+#pragma unroll 1
+  for (int c = c0; c < kBN / 64; ++c) {
+    uint32_t g[32], u[32];
+    tmem_ld32(taddr + c * 32, g);
+    tmem_ld32(taddr + kBN / 2 + c * 32, u);
+    tmem_ld_wait();
+    if (!EARLY) release_sf_cols(sf_bar, c);
+    chunk(c, g, u);
   }
 }
 
@@ -511,12 +562,12 @@ __global__ void __launch_bounds__(192, 1)
       const int row = mt * kBM + row_in_tile;
       uint64_t* sf_bar = MX ? &sffree[acc] : nullptr;
       if (KIND == kEpiQkv)
-        epi_qkv(p, taddr, row, n0, ncols, sf_bar);
+        epi_qkv<MX>(p, taddr, row, n0, ncols, sf_bar);
       else if (KIND == kEpiResid)
         epi_resid(p, taddr, mt * kBM + quarter * 32, lane, n0, ncols,
                   reinterpret_cast<float*>(smem + kStages * G::kStage + 256) + (warp - 2) * 32 * 33, sf_bar);
       else if (KIND == kEpiSwiglu)
-        epi_swiglu(p, taddr, row, nt * kBN, sf_bar);  // never split: a tile pairs gate and up columns
+        epi_swiglu<MX>(p, taddr, row, nt * kBN, sf_bar);  // never split: a tile pairs gate and up columns
       else
         epi_f32(p, taddr, row, n0, ncols, sf_bar);
       tc_fence_before();
@@ -728,12 +779,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN;
       const int row = mt * kPairRows + row_in_tile;
       if (KIND == kEpiQkv)
-        epi_qkv(p, taddr, row, n0, ncols, nullptr);
+        epi_qkv<false>(p, taddr, row, n0, ncols, nullptr);
       else if (KIND == kEpiResid)
         epi_resid(p, taddr, row - lane, lane, n0, ncols,
                   reinterpret_cast<float*>(smem + kPairStages * kPairStage + 256) + (warp - 2) * 32 * 33, nullptr);
       else if (KIND == kEpiSwiglu)
-        epi_swiglu(p, taddr, row, nt * kBN, nullptr);  // never split: a tile pairs gate and up columns
+        epi_swiglu<false>(p, taddr, row, nt * kBN, nullptr);  // never split: a tile pairs gate and up columns
       else
         epi_f32(p, taddr, row, n0, ncols, nullptr);
       tc_fence_before();
