@@ -37,7 +37,7 @@ SYMBOLS = (
     "qi_dit_create", "qi_dit_destroy", "qi_dit_load_global", "qi_dit_load_block",
     "qi_rope_axis_tables", "qi_rope_tables", "qi_flow_sigmas", "qi_pack_noise", "qi_euler_update",
     "qi_dit_step", "qi_text_kv_capture", "qi_kv_cache_bytes", "qi_dit_check",
-    "qi_dit_block_forward", "qi_dit_read_kv", "qi_dit_set_trace", "qi_dit_profile",
+    "qi_dit_block_forward", "qi_dit_read_kv", "qi_dit_set_trace", "qi_dit_profile", "qi_dit_profile_classes",
     "qi_dit_profile_read", "qi_last_error", "qi_gemm_bf16", "qi_attention_f16", "qi_gemm_bf16_noalloc",
     "qi_dit_step_cfg", "qi_dpmpp2m_coeffs", "qi_dpmpp2m_update", "qi_dit_step_fbcache", "qi_dit_fbcache_reset",
     "qi_dit_set_mxfp8", "qi_quant_mxfp8", "qi_gemm_mxfp8", "qi_debug_inject",
@@ -103,6 +103,7 @@ def lib() -> ctypes.CDLL:
         "qi_dit_read_kv": [P, I, I, I, P, P, P],
         "qi_dit_set_trace": [P, I, I, P],
         "qi_dit_profile": [P, I],
+        "qi_dit_profile_classes": [P, U],
         "qi_dit_profile_read": [P, P, P],
         "qi_gemm_bf16": [P, P, P, P, I, I, I, P],
         "qi_attention_f16": [P, P, P, P, I, I, I, I, P],
@@ -461,8 +462,18 @@ class DiT:
     def check(self, stream=None):
         _check(lib().qi_dit_check(self._h, _stream(stream)))
 
-    def profile(self, enable: bool):
-        _check(lib().qi_dit_profile(self._h, int(enable)))
+    def profile(self, enable: bool, classes=None):
+        """Time kernel classes with CUDA events: all of them (classes None), or only
+        the named ones (names from PROF_CLASSES); enable False turns timing off."""
+        if not enable:
+            _check(lib().qi_dit_profile(self._h, 0))
+        elif classes is None:
+            _check(lib().qi_dit_profile(self._h, 1))
+        else:
+            mask = 0
+            for c in classes:
+                mask |= 1 << PROF_CLASSES.index(c)
+            _check(lib().qi_dit_profile_classes(self._h, mask))
 
     def profile_read(self) -> dict:
         ms = (ctypes.c_double * len(PROF_CLASSES))()

@@ -202,7 +202,7 @@ struct qi_dit {
   int trace_block[2] = {-1, -1};
   float* trace_dst[2] = {nullptr, nullptr};
 
-  bool prof = false;
+  unsigned prof_mask = 0;  // kernel classes timed with events (bit c = class c)
   struct ProfEv {
     int cls;
     cudaEvent_t a, b;
@@ -225,7 +225,7 @@ struct ProfScope {
   int cls;
   qi_dit::ProfEv* ev = nullptr;
   ProfScope(qi_dit* d_, cudaStream_t s_, int c) : d(d_), s(s_), cls(c) {
-    if (!d->prof) return;
+    if (!((d->prof_mask >> c) & 1u)) return;
     if (d->prof_used == d->prof_ev.size()) {
       qi_dit::ProfEv e{c, nullptr, nullptr};
       cudaEventCreate(&e.a);
@@ -1317,7 +1317,16 @@ qi_status qi_dit_set_trace(qi_dit* d, int slot, int block, float* dst) {
 
 qi_status qi_dit_profile(qi_dit* d, int enable) {
   if (!d) return fail(QI_ERR_INVALID_ARG, "qi_dit_profile: NULL handle");
-  d->prof = enable != 0;
+  d->prof_mask = enable != 0 ? (1u << QI_PROF_CLASSES) - 1u : 0u;
+  d->prof_used = 0;
+  return QI_OK;
+}
+
+qi_status qi_dit_profile_classes(qi_dit* d, unsigned mask) {
+  if (!d) return fail(QI_ERR_INVALID_ARG, "qi_dit_profile_classes: NULL handle");
+  if (mask >> QI_PROF_CLASSES) return fail(QI_ERR_INVALID_ARG, "qi_dit_profile_classes: mask 0x%x has bits past class %d",
+                                            mask, QI_PROF_CLASSES - 1);
+  d->prof_mask = mask;
   d->prof_used = 0;
   return QI_OK;
 }

@@ -68,6 +68,30 @@ def dit256(qi):
     d.close()
 
 
+def test_profile_classes_selects_kernel_classes(qi, dit256):
+    """Class-selective timing: only the named classes record launches (one gate/up GEMM
+    per block), every class when enabled without names, nothing when off; a mask bit
+    past the last class is rejected."""
+    case, W, d = dit256
+    img = f32_tensor(synth.img_tokens(case))
+    txt = f32_tensor(synth.txt_feats(case))
+    tabs = [f32_tensor(a) for a in _tables(case.L, case.h, case.w)]
+    d.profile(True, classes=["gateup_gemm"])
+    d.step(img, txt, case.timestep, *tabs)
+    prof = d.profile_read()
+    assert prof["gateup_gemm"][1] == 32 and prof["gateup_gemm"][0] > 0
+    assert all(n == 0 for c, (_, n) in prof.items() if c != "gateup_gemm")
+    d.profile(True)
+    d.step(img, txt, case.timestep, *tabs)
+    prof = d.profile_read()
+    assert all(n > 0 for _, n in prof.values())
+    d.profile(False)
+    d.step(img, txt, case.timestep, *tabs)
+    assert all(n == 0 for _, n in d.profile_read().values())
+    assert qi.lib().qi_dit_profile_classes(d._h, 1 << len(qi.PROF_CLASSES)) == 1
+    d.check()
+
+
 def test_step_256(qi, dit256):
     case, W, d = dit256
     img = synth.img_tokens(case)
