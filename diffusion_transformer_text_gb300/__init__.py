@@ -103,7 +103,7 @@ def lib() -> ctypes.CDLL:
         "qi_dit_read_kv": [P, I, I, I, P, P, P],
         "qi_dit_set_trace": [P, I, I, P],
         "qi_dit_profile": [P, I],
-        "qi_dit_profile_classes": [P, U],
+        "qi_dit_profile_classes": [P, U, I],
         "qi_dit_profile_read": [P, P, P],
         "qi_gemm_bf16": [P, P, P, P, I, I, I, P],
         "qi_attention_f16": [P, P, P, P, I, I, I, I, P],
@@ -462,18 +462,19 @@ class DiT:
     def check(self, stream=None):
         _check(lib().qi_dit_check(self._h, _stream(stream)))
 
-    def profile(self, enable: bool, classes=None):
+    def profile(self, enable: bool, classes=None, block_stride: int = 1):
         """Time kernel classes with CUDA events: all of them (classes None), or only
-        the named ones (names from PROF_CLASSES); enable False turns timing off."""
+        the named ones (names from PROF_CLASSES), the per-block ones only in blocks
+        b % block_stride == 0; enable False turns timing off."""
         if not enable:
             _check(lib().qi_dit_profile(self._h, 0))
-        elif classes is None:
+        elif classes is None and block_stride == 1:
             _check(lib().qi_dit_profile(self._h, 1))
         else:
             mask = 0
-            for c in classes:
+            for c in (PROF_CLASSES if classes is None else classes):
                 mask |= 1 << PROF_CLASSES.index(c)
-            _check(lib().qi_dit_profile_classes(self._h, mask))
+            _check(lib().qi_dit_profile_classes(self._h, mask, int(block_stride)))
 
     def profile_read(self) -> dict:
         ms = (ctypes.c_double * len(PROF_CLASSES))()

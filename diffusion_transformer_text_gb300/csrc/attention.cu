@@ -102,6 +102,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the set-up above may overlap the previous kernel; every activation read and
+  // write comes after this wait
+  grid_dep_wait();
+  grid_dep_launch_dependents();
   const uint32_t tO = tmem + kOCol;
 
   if (warp == 0 || warp == 6) {
@@ -353,8 +357,7 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kHeadDim));
   dim3 grid((p.Rq + kBQ - 1) / kBQ, kHeads);
-  attn_tc<<<grid, kThreads, kSmem, stream>>>(mq, mk, mv, p, scale_log2);
-  return cudaGetLastError();
+  return launch_dependent(attn_tc, grid, dim3(kThreads), kSmem, stream, mq, mk, mv, p, scale_log2);
 }
 
 }  // namespace qi

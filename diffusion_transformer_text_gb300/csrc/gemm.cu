@@ -417,6 +417,10 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the set-up above may overlap the previous kernel; every activation read and
+  // write comes after this wait
+  grid_dep_wait();
+  grid_dep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -658,6 +662,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the set-up above may overlap the previous kernel; every activation read and
+  // write comes after this wait
+  grid_dep_wait();
+  grid_dep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -825,8 +833,7 @@ cudaError_t launch_pair_kind(const CUtensorMap& a, const CUtensorMap& b, const G
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_pair_tc<KIND><<<grid, 192, kPairSmem, stream>>>(a, b, p);
-  return cudaGetLastError();
+  return launch_dependent(gemm_pair_tc<KIND>, dim3(grid), dim3(192), kPairSmem, stream, a, b, p);
 }
 
 cudaError_t launch_pair_any(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
@@ -866,8 +873,7 @@ cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmPa
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_bf16_tc<KIND, MX><<<grid, 192, Geo<MX>::kSmem, stream>>>(a, b, p);
-  return cudaGetLastError();
+  return launch_dependent(gemm_bf16_tc<KIND, MX>, dim3(grid), dim3(192), Geo<MX>::kSmem, stream, a, b, p);
 }
 
 template <bool MX>

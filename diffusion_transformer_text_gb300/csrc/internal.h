@@ -106,6 +106,27 @@ struct GemmParams {
 // Launch one persistent tcgen05 GEMM D[M,N] = A[M,K] * B[N,K]^T with the
 // epilogue `kind`. A and B maps are 2-D 16-bit maps with box {64, 128} /
 // {64, 256}; the operands are fp16 for the DiT epilogues and bf16 for kEpiF32.
+// Launch with programmatic stream serialization: the kernel's set-up (barrier
+// initialisation, TMEM allocation, tensor-map prefetch) overlaps the end of the
+// previous kernel in the stream. Only kernels that execute grid_dep_wait()
+// before touching any activation (read or write) are launched this way, so each
+// one still sees all earlier work complete; other kernels launch normally.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 cudaError_t launch_gemm(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                         int grid_ctas, cudaStream_t stream);
 

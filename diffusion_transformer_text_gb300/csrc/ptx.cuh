@@ -114,6 +114,19 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
+// ------------------------------------------------------------------ dependent launch
+//
+// A kernel launched with programmatic stream serialization may start while the
+// previous kernel in the stream is still running. griddepcontrol.wait blocks until
+// that kernel has completed and its memory operations are visible (immediately if
+// there is no such dependency); launch_dependents lets the next kernel in the
+// stream begin launching once every CTA of this grid has issued it (or exited).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 
 // Allocate `ncols` TMEM columns (power of two >= 32); whole warp; address -> *slot.

@@ -203,6 +203,7 @@ struct qi_dit {
   float* trace_dst[2] = {nullptr, nullptr};
 
   unsigned prof_mask = 0;  // kernel classes timed with events (bit c = class c)
+  int prof_stride = 1;     // block-level classes: only blocks b % prof_stride == 0
   struct ProfEv {
     int cls;
     cudaEvent_t a, b;
@@ -224,8 +225,10 @@ struct ProfScope {
   cudaStream_t s;
   int cls;
   qi_dit::ProfEv* ev = nullptr;
-  ProfScope(qi_dit* d_, cudaStream_t s_, int c) : d(d_), s(s_), cls(c) {
+  // block: the block index of a per-block launch group (-1 for the rest)
+  ProfScope(qi_dit* d_, cudaStream_t s_, int c, int block = -1) : d(d_), s(s_), cls(c) {
     if (!((d->prof_mask >> c) & 1u)) return;
+    if (block >= 0 && block % d->prof_stride != 0) return;
     if (d->prof_used == d->prof_ev.size()) {
       qi_dit::ProfEv e{c, nullptr, nullptr};
       cudaEventCreate(&e.a);
@@ -317,7 +320,7 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
 
   // QKV + 1/rms + RoPE -> Q and this block's K/V store
   {
-    ProfScope ps(d, s, 0);
+    ProfScope ps(d, s, 0, b);
     qi::GemmParams g = p;
     g.N = 3 * kHidden;
     g.K = kHidden;
@@ -346,7 +349,7 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
   }
   // block-causal attention
   {
-    ProfScope ps(d, s, 1);
+    ProfScope ps(d, s, 1, b);
     qi::AttnParams a{};
     a.q = d->q;
     a.k = two.split > 0 ? d->k_at(0, b) : d->k_of(b);
@@ -382,7 +385,7 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
   }
   // out-projection: x += g1 * (o Wo^T); xa = fp16(x (1 + s2))
   {
-    ProfScope ps(d, s, 2);
+    ProfScope ps(d, s, 2, b);
     qi::GemmParams g = p;
     g.N = kHidden;
     g.K = kHidden;
@@ -397,7 +400,7 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
   }
   // gate/up + SwiGLU
   {
-    ProfScope ps(d, s, 3);
+    ProfScope ps(d, s, 3, b);
     qi::GemmParams g = p;
     g.N = 2 * kFfn;
     g.K = kHidden;
@@ -413,7 +416,7 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
   }
   // down: x += g2 * (h Wd^T); xa = fp16(x (1 + s1)) for the next block
   {
-    ProfScope ps(d, s, 4);
+    ProfScope ps(d, s, 4, b);
     qi::GemmParams g = p;
     g.N = kHidden;
     g.K = kFfn;
@@ -1318,15 +1321,18 @@ qi_status qi_dit_set_trace(qi_dit* d, int slot, int block, float* dst) {
 qi_status qi_dit_profile(qi_dit* d, int enable) {
   if (!d) return fail(QI_ERR_INVALID_ARG, "qi_dit_profile: NULL handle");
   d->prof_mask = enable != 0 ? (1u << QI_PROF_CLASSES) - 1u : 0u;
+  d->prof_stride = 1;
   d->prof_used = 0;
   return QI_OK;
 }
 
-qi_status qi_dit_profile_classes(qi_dit* d, unsigned mask) {
+qi_status qi_dit_profile_classes(qi_dit* d, unsigned mask, int block_stride) {
   if (!d) return fail(QI_ERR_INVALID_ARG, "qi_dit_profile_classes: NULL handle");
   if (mask >> QI_PROF_CLASSES) return fail(QI_ERR_INVALID_ARG, "qi_dit_profile_classes: mask 0x%x has bits past class %d",
                                             mask, QI_PROF_CLASSES - 1);
+  if (block_stride < 1) return fail(QI_ERR_INVALID_ARG, "qi_dit_profile_classes: block_stride %d < 1", block_stride);
   d->prof_mask = mask;
+  d->prof_stride = block_stride;
   d->prof_used = 0;
   return QI_OK;
 }

@@ -420,14 +420,17 @@ qi_status qi_dit_set_trace(qi_dit* dit, int slot, int block, float* dst);
 /* Per-kernel-class device time, measured with CUDA events on the launching
  * stream while enabled. Classes: 0 QKV GEMM, 1 attention, 2 out-proj GEMM,
  * 3 gate/up GEMM, 4 down GEMM, 5 other. Each timed launch group adds two event
- * records to the stream (about 1-2 us each), so timing every class slows a pass
- * by roughly 1 %. qi_dit_profile: enable != 0 times every class, 0 none.
- * qi_dit_profile_classes: times only the classes whose bit (1 << class) is set
- * in `mask` (0 = none); bits at or above QI_PROF_CLASSES give QI_ERR_INVALID_ARG.
- * Either call resets the counters. */
+ * records to the stream, and an event between two kernels also stops the second
+ * from starting its set-up under the first, so timing every class slows a pass
+ * by roughly 1 %. qi_dit_profile: enable != 0 times every class in every block,
+ * 0 none. qi_dit_profile_classes: times only the classes whose bit (1 << class)
+ * is set in `mask` (0 = none), and the per-block classes 0-4 only in blocks b
+ * with b % block_stride == 0 (1 = every block). Bits at or above
+ * QI_PROF_CLASSES or block_stride < 1 give QI_ERR_INVALID_ARG. Either call
+ * resets the counters. */
 #define QI_PROF_CLASSES 6
 qi_status qi_dit_profile(qi_dit* dit, int enable);
-qi_status qi_dit_profile_classes(qi_dit* dit, unsigned mask);
+qi_status qi_dit_profile_classes(qi_dit* dit, unsigned mask, int block_stride);
 /* Synchronises; writes total milliseconds and launch counts per class since
  * the last reset, then resets. ms/launches: host arrays [QI_PROF_CLASSES]. */
 qi_status qi_dit_profile_read(qi_dit* dit, double* ms, long long* launches);

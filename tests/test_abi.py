@@ -96,7 +96,7 @@ def test_status_codes(qi):
     assert L.qi_dit_step(None, None, 8, None, 8, 0.5, None, None, None, None, None, 0, None) == 1
     assert L.qi_attention_f16(None, None, None, None, 1, 0, 1, 1, None) == 1
     assert L.qi_dit_profile(None, 1) == 1
-    assert L.qi_dit_profile_classes(None, 8) == 1
+    assert L.qi_dit_profile_classes(None, 8, 1) == 1
 
 
 def test_kv_slots_range(qi):

@@ -70,8 +70,9 @@ def dit256(qi):
 
 def test_profile_classes_selects_kernel_classes(qi, dit256):
     """Class-selective timing: only the named classes record launches (one gate/up GEMM
-    per block), every class when enabled without names, nothing when off; a mask bit
-    past the last class is rejected."""
+    per block, or per fourth block with a stride of 4), every class when enabled without
+    names, nothing when off; a mask bit past the last class or a stride below 1 is
+    rejected."""
     case, W, d = dit256
     img = f32_tensor(synth.img_tokens(case))
     txt = f32_tensor(synth.txt_feats(case))
@@ -81,6 +82,11 @@ def test_profile_classes_selects_kernel_classes(qi, dit256):
     prof = d.profile_read()
     assert prof["gateup_gemm"][1] == 32 and prof["gateup_gemm"][0] > 0
     assert all(n == 0 for c, (_, n) in prof.items() if c != "gateup_gemm")
+    d.profile(True, classes=["gateup_gemm", "attention"], block_stride=4)
+    d.step(img, txt, case.timestep, *tabs)
+    prof = d.profile_read()
+    assert prof["gateup_gemm"][1] == 8 and prof["attention"][1] == 8
+    assert all(n == 0 for c, (_, n) in prof.items() if c not in ("gateup_gemm", "attention"))
     d.profile(True)
     d.step(img, txt, case.timestep, *tabs)
     prof = d.profile_read()
@@ -88,7 +94,8 @@ def test_profile_classes_selects_kernel_classes(qi, dit256):
     d.profile(False)
     d.step(img, txt, case.timestep, *tabs)
     assert all(n == 0 for _, n in d.profile_read().values())
-    assert qi.lib().qi_dit_profile_classes(d._h, 1 << len(qi.PROF_CLASSES)) == 1
+    assert qi.lib().qi_dit_profile_classes(d._h, 1 << len(qi.PROF_CLASSES), 1) == 1
+    assert qi.lib().qi_dit_profile_classes(d._h, 8, 0) == 1
     d.check()
 
 
