@@ -227,8 +227,12 @@ __device__ __forceinline__ void epi_resid(const GemmParams& p, uint32_t taddr, i
   float sq[32];
 #pragma unroll
   for (int rr = 0; rr < 32; ++rr) sq[rr] = 0.f;
+  const bool own_row = !p.resid_set && row0 + lane < p.M;
 #pragma unroll 1
   for (int c = 0; c < ncols / 32; ++c) {
+    // the next chunk's residual segment of this lane's row (one 128-byte line) into L1
+    if (own_row && c + 1 < ncols / 32)
+      prefetch_l1(p.x + static_cast<size_t>(row0 + lane) * kHidden + n0 + (c + 1) * 32);
     uint32_t r[32];
     tmem_ld32(taddr + c * 32, r);
     tmem_ld_wait();
