@@ -6,7 +6,7 @@
 // from the bf16 checkpoint values; [out, in] row-major), fp32 accumulation in
 // tensor memory. The plain fp32 epilogue (a test hook) takes bf16 operands.
 //
-// MXFP8 variant (MX = true): A and B are E4M3 bytes with one UE8M0 scale per 32
+// MXFP8 kernel (gemm_mx_tc): A and B are E4M3 bytes with one UE8M0 scale per 32
 // values along K, stored in 512-byte chunks (128 rows x 4 scales, byte
 // (r % 32) * 16 + ((r % 128) / 32) * 4 + k) ordered [K / 128][rows / 128]. A
 // stage then covers K = 128; its scale chunks arrive by bulk copy with the
@@ -19,14 +19,16 @@
 // Two kernels share the epilogues. The fp16 / bf16 GEMMs run on CTA pairs
 // (gemm_pair_tc: a cluster of two CTAs computes 256 x 256 tiles with
 // tcgen05.mma.cta_group::2, each CTA loading its 128 A rows and half of the B
-// rows); the MXFP8 GEMM runs one CTA per 128 x 256 tile (gemm_bf16_tc).
+// rows); the MXFP8 GEMM runs one CTA per 128 x 256 tile (gemm_mx_tc).
 //
 // Roles per CTA (192 threads):
-//   warp 0     TMA producer: A and B tiles into a ring of stages (pair: 128x64 A
-//              and 128x64 B, 6 stages; single: 128x64 A and 256x64 B, 4 stages)
+//   warp 0     TMA producer: A and B tiles into a ring of stages (pair: 128x64
+//              fp16 A and 128x64 fp16 B, 6 stages; MXFP8: 128x128 E4M3 A, 256x128
+//              E4M3 B and the scale chunks, 4 stages)
 //   warp 1     TMEM owner and MMA issuer (one thread; the pair's leader only):
-//              4 x tcgen05.mma per stage (K = 16 each; M = 256 across the pair or
-//              128), accumulating into one of two 256-column TMEM buffers
+//              4 x tcgen05.mma per stage (pair: M = 256, K = 16 each; MXFP8:
+//              M = 128, K = 32 each), accumulating into one of two 256-column
+//              TMEM buffers
 //   warps 2-5  epilogue: each thread owns one accumulator row (TMEM lane),
 //              reads 32 columns at a time and applies the fused epilogue while
 //              the MMA warp fills the other TMEM buffer.
@@ -46,21 +48,20 @@
 namespace qi {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kMxStages = 4;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;  // 32 KB
 constexpr int kEpiScratch = 4 * 32 * 33 * 4;  // per epilogue warp: one 32 x 32 fp32 chunk, stride 33
 constexpr int kSfChunk = 512;                  // MXFP8 scales of 128 rows x 128 K
 
-// Per-variant geometry: the tile bytes are the same (128-byte rows), MXFP8 packs
-// twice the K per stage and adds the scale chunks of A (one) and B (two).
-template <bool MX>
-struct Geo {
-  static constexpr int kSF = MX ? 3 * kSfChunk : 0;
+// MXFP8 kernel geometry: 128-byte tile rows as for 16-bit operands, so a stage
+// packs K = 128 E4M3 values and adds the scale chunks of A (one) and B (two).
+struct MxGeo {
+  static constexpr int kSF = 3 * kSfChunk;
   static constexpr int kStage = kABytes + kBBytes + kSF;
-  static constexpr int kK = MX ? 128 : kBK;  // K elements per stage
-  static constexpr int kAcc = 2;             // TMEM accumulators (256 columns each)
-  static constexpr int kSmem = kStages * kStage + 1024 + 256 + kEpiScratch;
+  static constexpr int kK = 128;  // K elements per stage
+  static constexpr int kAcc = 2;  // TMEM accumulators (256 columns each)
+  static constexpr int kSmem = kMxStages * kStage + 1024 + 256 + kEpiScratch;
 };
 // MXFP8: a tile's stage-s scales sit at columns 16 s (A: +0..3, B: +4..11) of the OTHER
 // accumulator, i.e. inside the tile the epilogue is draining.
@@ -87,12 +88,6 @@ __device__ __forceinline__ void unit_tile(int u, int tail_start, int& tile, int&
     tile = tail_start + ((u - tail_start) >> 1);
     half = (u - tail_start) & 1;
   }
-}
-
-template <int KIND, bool MX>
-__device__ __forceinline__ uint32_t idesc_for(int n, uint32_t k) {
-  if (MX) return idesc_mxf8_f32(kBM, n, k);
-  return KIND == kEpiF32 ? idesc_bf16_f32(kBM, n) : idesc_f16_f32(kBM, n);
 }
 
 __device__ __forceinline__ float row_rinv(const float* ssp, int row) {
@@ -366,19 +361,19 @@ __device__ __forceinline__ void epi_f32(const GemmParams& p, uint32_t taddr, int
 
 // ---------------------------------------------------------------- kernel
 
-template <int KIND, bool MX>
+template <int KIND>
 __global__ void __launch_bounds__(192, 1)
-    gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const GemmParams p) {
-  using G = Geo<MX>;
+    gemm_mx_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const GemmParams p) {
+  using G = MxGeo;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kABytes;
-  uint8_t* sSF = sB + kStages * kBBytes;  // MXFP8 scale chunks, G::kSF bytes per stage
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * G::kStage);
-  uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;
+  uint8_t* sB = smem + kMxStages * kABytes;
+  uint8_t* sSF = sB + kMxStages * kBBytes;  // MXFP8 scale chunks, G::kSF bytes per stage
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kMxStages * G::kStage);
+  uint64_t* empty = full + kMxStages;
+  uint64_t* tfull = empty + kMxStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint64_t* sffree = drain + 1;  // MXFP8: scale columns of accumulator a readable again
@@ -395,7 +390,7 @@ __global__ void __launch_bounds__(192, 1)
   const int kblocks = p.K / G::kK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kMxStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -447,25 +442,23 @@ __global__ void __launch_bounds__(192, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], G::kStage - (MX ? (2 - sfb_chunks) * kSfChunk : 0));
+          mbar_arrive_expect_tx(&full[stage], G::kStage - (2 - sfb_chunks) * kSfChunk);
           tma_load_2d(sA + stage * kABytes, &tmA, &full[stage], kb * G::kK, mt * kBM);
           tma_load_2d(sB + stage * kBBytes, &tmB, &full[stage], kb * G::kK, n_row);
-          if (MX) {
-            uint8_t* sf = sSF + stage * G::kSF;
-            bulk_load(sf, p.sfa + (static_cast<size_t>(kb) * num_m + mt) * kSfChunk, kSfChunk, &full[stage]);
-            bulk_load(sf + kSfChunk, p.sfb + (static_cast<size_t>(kb) * (p.N / 128) + n_row / 128) * kSfChunk,
-                      sfb_chunks * kSfChunk, &full[stage]);
-          }
+          uint8_t* sf = sSF + stage * G::kSF;
+          bulk_load(sf, p.sfa + (static_cast<size_t>(kb) * num_m + mt) * kSfChunk, kSfChunk, &full[stage]);
+          bulk_load(sf + kSfChunk, p.sfb + (static_cast<size_t>(kb) * (p.N / 128) + n_row / 128) * kSfChunk,
+                    sfb_chunks * kSfChunk, &full[stage]);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) {
+          if (++stage == kMxStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
       // every load this thread issued must land before the CTA may exit
-      for (int s = 0; s < kStages; ++s)
+      for (int s = 0; s < kMxStages; ++s)
         if ((issued_mask >> s) & 1u)
           if (!mbar_wait(&full[s], (issued_parity >> s) & 1u)) report_error(p.err, kErrTimeoutDrain);
     }
@@ -487,7 +480,7 @@ __global__ void __launch_bounds__(192, 1)
           *abort_flag = 1;
           break;
         }
-        if (MX && local > 0) {
+        if (local > 0) {
           // the previous tile (other accumulator) must be complete, and its epilogue
           // past the first 64 columns, before this tile's scales go there
           const uint32_t prev_parity = static_cast<uint32_t>((local - 1) >> 1) & 1u;
@@ -512,26 +505,19 @@ __global__ void __launch_bounds__(192, 1)
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + stage * kABytes);
           const uint32_t b0 = smem_u32(sB + stage * kBBytes);
-          if (MX) {
-            // this stage's scale set: the MMAs that last read it (kStages stages ago)
-            // completed before the producer could refill the stage
-            const uint32_t sf_t = tmem_base + (acc ^ 1u) * kBN + 16 * stage;
-            const uint32_t sf_s = smem_u32(sSF + stage * G::kSF);
-            tmem_cp_sf(sf_t, plain_rows16_desc(sf_s));
-            tmem_cp_sf(sf_t + 4, plain_rows16_desc(sf_s + kSfChunk));
-            if (half_u < 0) tmem_cp_sf(sf_t + 8, plain_rows16_desc(sf_s + 2 * kSfChunk));
+          // this stage's scale set: the MMAs that last read it (kMxStages stages ago)
+          // completed before the producer could refill the stage
+          const uint32_t sf_t = tmem_base + (acc ^ 1u) * kBN + 16 * stage;
+          const uint32_t sf_s = smem_u32(sSF + stage * G::kSF);
+          tmem_cp_sf(sf_t, plain_rows16_desc(sf_s));
+          tmem_cp_sf(sf_t + 4, plain_rows16_desc(sf_s + kSfChunk));
+          if (half_u < 0) tmem_cp_sf(sf_t + 8, plain_rows16_desc(sf_s + 2 * kSfChunk));
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_mxf8(d, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k),
-                       idesc_for<KIND, MX>(n_mma, static_cast<uint32_t>(k)), sf_t, sf_t + 4, (kb | k) != 0 ? 1u : 0u);
-          } else {
-#pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              mma_ss(d, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k), idesc_for<KIND, MX>(n_mma, 0),
-                     (kb | k) != 0 ? 1u : 0u);
-          }
+          for (int k = 0; k < 4; ++k)
+            mma_mxf8(d, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k),
+                     idesc_mxf8_f32(kBM, n_mma, static_cast<uint32_t>(k)), sf_t, sf_t + 4, (kb | k) != 0 ? 1u : 0u);
           mma_commit(&empty[stage]);
-          if (++stage == kStages) {
+          if (++stage == kMxStages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -568,14 +554,14 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN;
       const int row = mt * kBM + row_in_tile;
-      uint64_t* sf_bar = MX ? &sffree[acc] : nullptr;
+      uint64_t* sf_bar = &sffree[acc];
       if (KIND == kEpiQkv)
-        epi_qkv<MX>(p, taddr, row, n0, ncols, sf_bar);
+        epi_qkv<true>(p, taddr, row, n0, ncols, sf_bar);
       else if (KIND == kEpiResid)
         epi_resid(p, taddr, mt * kBM + quarter * 32, lane, n0, ncols,
-                  reinterpret_cast<float*>(smem + kStages * G::kStage + 256) + (warp - 2) * 32 * 33, sf_bar);
+                  reinterpret_cast<float*>(smem + kMxStages * G::kStage + 256) + (warp - 2) * 32 * 33, sf_bar);
       else if (KIND == kEpiSwiglu)
-        epi_swiglu<MX>(p, taddr, row, nt * kBN, sf_bar);  // never split: a tile pairs gate and up columns
+        epi_swiglu<true>(p, taddr, row, nt * kBN, sf_bar);  // never split: a tile pairs gate and up columns
       else
         epi_f32(p, taddr, row, n0, ncols, sf_bar);
       tc_fence_before();
@@ -867,25 +853,23 @@ cudaError_t launch_pair_any(EpiKind kind, const CUtensorMap& a, const CUtensorMa
   return cudaErrorInvalidValue;
 }
 
-template <int KIND, bool MX>
-cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
-                        cudaStream_t stream) {
+template <int KIND>
+cudaError_t launch_mx_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
+                           cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(gemm_bf16_tc<KIND, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<MX>::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(gemm_mx_tc<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, MxGeo::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_dependent(gemm_bf16_tc<KIND, MX>, dim3(grid), dim3(192), Geo<MX>::kSmem, stream, a, b, p);
+  return launch_dependent(gemm_mx_tc<KIND>, dim3(grid), dim3(192), MxGeo::kSmem, stream, a, b, p);
 }
 
-template <bool MX>
-cudaError_t launch_any(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
-                       int grid_ctas, cudaStream_t stream) {
+cudaError_t launch_mx_any(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                          int grid_ctas, cudaStream_t stream) {
   if (p.M <= 0) return cudaSuccess;
-  if (p.N % kBN != 0 || p.K % Geo<MX>::kK != 0) return cudaErrorInvalidValue;
-  if (MX && (p.sfa == nullptr || p.sfb == nullptr)) return cudaErrorInvalidValue;
+  if (p.N % kBN != 0 || p.K % MxGeo::kK != 0) return cudaErrorInvalidValue;
+  if (p.sfa == nullptr || p.sfb == nullptr) return cudaErrorInvalidValue;
   const int tiles = ((p.M + kBM - 1) / kBM) * (p.N / kBN);
   // split the last wave's tiles into 128-column halves when they fill at most half the grid
   GemmParams q = p;
@@ -896,13 +880,13 @@ cudaError_t launch_any(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b,
   const int grid = units < grid_ctas ? units : grid_ctas;
   switch (kind) {
     case kEpiQkv:
-      return launch_kind<kEpiQkv, MX>(a, b, q, grid, stream);
+      return launch_mx_kind<kEpiQkv>(a, b, q, grid, stream);
     case kEpiResid:
-      return launch_kind<kEpiResid, MX>(a, b, q, grid, stream);
+      return launch_mx_kind<kEpiResid>(a, b, q, grid, stream);
     case kEpiSwiglu:
-      return launch_kind<kEpiSwiglu, MX>(a, b, q, grid, stream);
+      return launch_mx_kind<kEpiSwiglu>(a, b, q, grid, stream);
     case kEpiF32:
-      return launch_kind<kEpiF32, MX>(a, b, q, grid, stream);
+      return launch_mx_kind<kEpiF32>(a, b, q, grid, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -916,7 +900,7 @@ cudaError_t launch_gemm(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b
 
 cudaError_t launch_gemm_mx(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                            int grid_ctas, cudaStream_t stream) {
-  return launch_any<true>(kind, a, b, p, grid_ctas, stream);
+  return launch_mx_any(kind, a, b, p, grid_ctas, stream);
 }
 
 }  // namespace qi
