@@ -47,6 +47,26 @@ def test_gemm_matches_matmul(qi, small_dit, M, N, K):
     assert (np.abs(D - ref) <= bound).all(), float((np.abs(D - ref) / bound).max())
 
 
+@pytest.mark.parametrize("M,N,K", [
+    (1024, 5120, 256),   # 80 pair tiles: a full wave, then the rest as 128-column halves
+    (1024, 7424, 128),   # 116 tiles: the leftover fills more than half the pairs, stays whole
+    (2048, 8192, 128),   # 256 tiles: several waves per pair, accumulator reuse, halves at the end
+    (1000, 5120, 2048),  # ragged M (last pair half empty) over many k-blocks
+])
+def test_gemm_waves_and_tails(qi, small_dit, M, N, K):
+    """Shapes with more 256 x 256 tiles than CTA pairs on a GB300 (152 SMs = 76 pairs), so the
+    persistent schedule runs full tiles, repeated tiles per pair and the last-wave halves."""
+    A = synth.weight_bf16(14, M, (M, K), std=1.0)
+    B = synth.weight_bf16(15, N, (N, K), std=1.0)
+    D = small_dit.gemm(bf16_tensor(A), bf16_tensor(B)).cpu().numpy()
+    small_dit.check()
+    a = synth.bf16_bits_to_f32(A).astype(np.float64)
+    b = synth.bf16_bits_to_f32(B).astype(np.float64)
+    ref = a @ b.T
+    bound = 1e-5 * (np.abs(a) @ np.abs(b).T) + 1e-6
+    assert (np.abs(D - ref) <= bound).all(), float((np.abs(D - ref) / bound).max())
+
+
 def test_gemm_rows_independent_of_m(qi, small_dit):
     """A row's result does not depend on how many rows the pass has (exact)."""
     K = 4096
