@@ -177,8 +177,10 @@ cudaError_t launch_gemv2(const float* x, int in_dim, const uint16_t* W, const ui
 cudaError_t launch_txt_prenorm(const float* txt, int L, const uint16_t* w, act_t* out, cudaStream_t s);
 cudaError_t launch_img_in(const float* img, int N, const uint16_t* W, const uint16_t* b, const float* mod,
                           float* x, act_t* xa, float* ssp, cudaStream_t s);
-cudaError_t launch_head(const float* x, int N, const float* ssp, const uint16_t* W, const uint16_t* b, float* vel,
+// wt: the head weight as a k-major fp32 copy [4096][64] (launch_head_wt, once at load)
+cudaError_t launch_head(const float* x, int N, const float* ssp, const float* wt, const uint16_t* b, float* vel,
                         int* err, cudaStream_t s);
+cudaError_t launch_head_wt(const uint16_t* W, float* wt, cudaStream_t s);
 cudaError_t launch_block_prep(const float* x, int R, int n_text, const float* mod, act_t* xa, float* ssp,
                               cudaStream_t s);
 cudaError_t launch_euler(float* x, const float* vel, long long n, float s_i, float s_next, cudaStream_t s);

@@ -209,39 +209,72 @@ __global__ void __launch_bounds__(256) img_in_kernel(const float* __restrict__ i
 // ---------------------------------------------------------------- output head
 
 // vel[i] = (x[i] / rms(x[i])) . Wout^T + b, 4096 -> 64, with rms from the sum-of-squares
-// partials. Block: 16 rows x 64 outputs; K staged through shared memory 128 at a time.
-constexpr int kHeadRows = 16;
-constexpr int kHeadK = 128;
+// partials. Block: 32 rows x 64 outputs, thread: 2 rows x 4 outputs (a float2 of x and a
+// float4 of the k-major fp32 weight copy per k). K runs through shared memory 64 at a
+// time; the next chunk is fetched into registers while the current one is multiplied.
+// Each output sums its 4096 products in k order (one fma chain).
+constexpr int kHeadRows = 32;
+constexpr int kHeadK = 64;
+constexpr int kHeadXPer = kHeadRows * kHeadK / 256;      // x values a thread stages per chunk (8)
+constexpr int kHeadWPer = kHeadK * kPatch / 4 / 256;     // weight float4s a thread stages per chunk (4)
 __global__ void __launch_bounds__(256) head_kernel(const float* __restrict__ x, int N, const float* __restrict__ ssp,
-                                                   const uint16_t* __restrict__ W, const uint16_t* __restrict__ b,
+                                                   const float* __restrict__ wt, const uint16_t* __restrict__ b,
                                                    float* __restrict__ vel, int* err) {
-  __shared__ float wt[kHeadK][kPatch + 1];
-  __shared__ float xs[kHeadRows][kHeadK + 1];
+  __shared__ __align__(16) float xs[kHeadK][kHeadRows + 2];  // [k][row], even stride: float2 reads
+  __shared__ __align__(16) float ws[kHeadK][kPatch + 4];     // [k][output], float4 reads
   const int r0 = blockIdx.x * kHeadRows;
-  const int i = threadIdx.x >> 4;   // row in block
-  const int oq = threadIdx.x & 15;  // outputs oq + 16 j
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const int tr = threadIdx.x >> 4;  // rows 2 tr, 2 tr + 1
+  const int to = threadIdx.x & 15;  // outputs 4 to .. 4 to + 3
+  float xr[kHeadXPer];
+  float4 wr[kHeadWPer];
+  auto fetch = [&](int k0) {
+#pragma unroll
+    for (int i = 0; i < kHeadXPer; ++i) {
+      const int e = threadIdx.x + 256 * i;
+      const int r = e / kHeadK, k = e % kHeadK;
+      xr[i] = (r0 + r) < N ? x[static_cast<size_t>(r0 + r) * kHidden + k0 + k] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < kHeadWPer; ++i) {
+      const int e = threadIdx.x + 256 * i;
+      wr[i] = reinterpret_cast<const float4*>(wt + static_cast<size_t>(k0 + e / (kPatch / 4)) * kPatch)[e % (kPatch / 4)];
+    }
+  };
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  fetch(0);
 #pragma unroll 1
   for (int k0 = 0; k0 < kHidden; k0 += kHeadK) {
-    for (int e = threadIdx.x; e < kPatch * kHeadK; e += 256) {
-      const int o = e / kHeadK, k = e % kHeadK;
-      wt[k][o] = bf16_bits_to_float(W[static_cast<size_t>(o) * kHidden + k0 + k]);
+#pragma unroll
+    for (int i = 0; i < kHeadXPer; ++i) {
+      const int e = threadIdx.x + 256 * i;
+      xs[e % kHeadK][e / kHeadK] = xr[i];
     }
-    for (int e = threadIdx.x; e < kHeadRows * kHeadK; e += 256) {
-      const int r = e / kHeadK, k = e % kHeadK;
-      xs[r][k] = (r0 + r) < N ? x[static_cast<size_t>(r0 + r) * kHidden + k0 + k] : 0.f;
+#pragma unroll
+    for (int i = 0; i < kHeadWPer; ++i) {
+      const int e = threadIdx.x + 256 * i;
+      *reinterpret_cast<float4*>(&ws[e / (kPatch / 4)][4 * (e % (kPatch / 4))]) = wr[i];
     }
     __syncthreads();
-#pragma unroll 8
+    if (k0 + kHeadK < kHidden) fetch(k0 + kHeadK);
+#pragma unroll 16
     for (int k = 0; k < kHeadK; ++k) {
-      const float xv = xs[i][k];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[j] += xv * wt[k][oq + 16 * j];
+      const float2 xv = *reinterpret_cast<const float2*>(&xs[k][2 * tr]);
+      const float4 wv = *reinterpret_cast<const float4*>(&ws[k][4 * to]);
+      acc[0][0] = fmaf(xv.x, wv.x, acc[0][0]);
+      acc[0][1] = fmaf(xv.x, wv.y, acc[0][1]);
+      acc[0][2] = fmaf(xv.x, wv.z, acc[0][2]);
+      acc[0][3] = fmaf(xv.x, wv.w, acc[0][3]);
+      acc[1][0] = fmaf(xv.y, wv.x, acc[1][0]);
+      acc[1][1] = fmaf(xv.y, wv.y, acc[1][1]);
+      acc[1][2] = fmaf(xv.y, wv.z, acc[1][2]);
+      acc[1][3] = fmaf(xv.y, wv.w, acc[1][3]);
     }
     __syncthreads();
   }
-  const int row = r0 + i;
-  if (row < N) {
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const int row = r0 + 2 * tr + rr;
+    if (row >= N) continue;
     const float4* p = reinterpret_cast<const float4*>(ssp + static_cast<size_t>(row) * kSspParts);
     float s = 0.f;
 #pragma unroll
@@ -255,13 +288,18 @@ __global__ void __launch_bounds__(256) head_kernel(const float* __restrict__ x, 
     const float rinv = rsqrtf(s * (1.f / kHidden) + kEps);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int o = oq + 16 * j;
-      const float v = acc[j] * rinv + bf16_bits_to_float(b[o]);
-      vel[static_cast<size_t>(row) * kPatch + o] = v;
+      const float v = acc[rr][j] * rinv + bf16_bits_to_float(b[4 * to + j]);
+      vel[static_cast<size_t>(row) * kPatch + 4 * to + j] = v;  // the caller's buffer: 4-byte aligned only
       // guard: a non-finite velocity (e.g. an fp16 operand that left its range) is reported
       if (!isfinite(v)) report_error(err, kErrNonFinite);
     }
   }
+}
+
+// The output head's weight [64][4096] bf16 as a k-major fp32 copy [4096][64] (once at load).
+__global__ void head_wt_kernel(const uint16_t* __restrict__ W, float* __restrict__ wt) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < kHidden * kPatch) wt[i] = bf16_bits_to_float(W[static_cast<size_t>(i % kPatch) * kHidden + i / kPatch]);
 }
 
 // ---------------------------------------------------------------- RoPE tables
@@ -598,10 +636,15 @@ cudaError_t launch_img_in(const float* img, int N, const uint16_t* W, const uint
   return cudaGetLastError();
 }
 
-cudaError_t launch_head(const float* x, int N, const float* ssp, const uint16_t* W, const uint16_t* b, float* vel,
+cudaError_t launch_head(const float* x, int N, const float* ssp, const float* wt, const uint16_t* b, float* vel,
                         int* err, cudaStream_t s) {
   if (N <= 0) return cudaSuccess;
-  head_kernel<<<(N + kHeadRows - 1) / kHeadRows, 256, 0, s>>>(x, N, ssp, W, b, vel, err);
+  head_kernel<<<(N + kHeadRows - 1) / kHeadRows, 256, 0, s>>>(x, N, ssp, wt, b, vel, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_head_wt(const uint16_t* W, float* wt, cudaStream_t s) {
+  head_wt_kernel<<<(kHidden * kPatch + 255) / 256, 256, 0, s>>>(W, wt);
   return cudaGetLastError();
 }
 

@@ -163,7 +163,8 @@ struct qi_dit {
   void* amem = nullptr;
   float* x = nullptr;      // [R_max, 4096] fp32 residual stream
   act_t* xa = nullptr;     // [R_max, 4096] fp16 modulated GEMM input
-  float* ssp = nullptr;    // [R_max, 16] sum-of-squares partials
+  float* ssp = nullptr;    // [R_max, 32] sum-of-squares partials (per 128 columns)
+  float* out_wt = nullptr; // [4096, 64] the output head's weight, k-major fp32
   act_t* q = nullptr;      // [R_max, 4096]
   act_t* o = nullptr;      // [R_max, 4096] attention output
   act_t* h = nullptr;      // [R_max, 12288] SwiGLU hidden
@@ -506,7 +507,7 @@ qi_status pass_head(qi_dit* d, const PassRows& pr, int N, float* vel, cudaStream
   if (pr.n_img == 0) return QI_OK;
   ProfScope ps(d, s, 5);
   const size_t off = static_cast<size_t>(pr.n_text);
-  QI_CUDA(qi::launch_head(d->x + off * kHidden, N, d->ssp + off * kSspParts, d->out_w, d->out_b, vel, d->err, s));
+  QI_CUDA(qi::launch_head(d->x + off * kHidden, N, d->ssp + off * kSspParts, d->out_wt, d->out_b, vel, d->err, s));
   return QI_OK;
 }
 
@@ -534,7 +535,7 @@ qi_status run_pass_two(qi_dit* d, const float* img, int N, float t, int L1, cons
   for (int b = 0; b < d->blocks; ++b) QI_TRY(run_block(d, b, R, 0, L1, L1, L1 + N, nullptr, nullptr, ic1, is1, s, two));
   {
     ProfScope ps(d, s, 5);
-    QI_CUDA(qi::launch_head(d->x, R, d->ssp, d->out_w, d->out_b, vel2, d->err, s));
+    QI_CUDA(qi::launch_head(d->x, R, d->ssp, d->out_wt, d->out_b, vel2, d->err, s));
   }
   return QI_OK;
 }
@@ -682,6 +683,7 @@ qi_status qi_dit_create(const qi_dit_config* cfg, int device, qi_dit** out) {
       {(void**)&d->txt_a, (size_t)d->L_max * kHidden * 2}, {(void**)&d->temb_e, 2 * kTdim * 4},
       {(void**)&d->temb_h, 2 * kHidden * 4}, {(void**)&d->temb, 2 * kHidden * 4},
       {(void**)&d->mod, 2 * (size_t)kMod * 4}, {(void**)&d->err, 256}, {(void**)&d->ovf, 256},
+      {(void**)&d->out_wt, (size_t)kHidden * kPatch * 4},
       {(void**)&d->kv, (size_t)d->slots * cfg->blocks * 2 * d->R_max * kHidden * 2},
       {(void**)&d->vel_pos, d->slots == 2 ? 2 * (size_t)d->N_max * kPatch * 4 : 0},
       {(void**)&d->vel_neg, d->slots == 2 ? (size_t)d->N_max * kPatch * 4 : 0},
@@ -816,6 +818,8 @@ qi_status qi_dit_load_global(qi_dit* d, const qi_global_weights* w, int src_on_d
   QI_CUDA(cudaSetDevice(d->device));
   const cudaMemcpyKind kind = src_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
   for (int i = 0; i < 13; ++i) QI_CUDA(cudaMemcpyAsync(dst[i], src[i], n[i] * 2, kind, s));
+  // the output head reads its weight as a k-major fp32 copy
+  QI_CUDA(qi::launch_head_wt(d->out_w, d->out_wt, s));
   // the text projection runs on the tensor cores with fp16 operands
   QI_TRY(convert_weights(d, {{d->txt_w, (size_t)kHidden * kHidden}}, s, "qi_dit_load_global"));
   d->loaded_global = true;
