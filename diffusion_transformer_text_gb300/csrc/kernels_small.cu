@@ -48,31 +48,42 @@ __global__ void __launch_bounds__(256) gemv2_kernel(const float* __restrict__ x,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int o_base = (blockIdx.x * 8 + warp) * kOutPerWarp;
   const int chunks = in_dim / 8;
-#pragma unroll 1
-  for (int j = 0; j < kOutPerWarp; ++j) {
-    const int o = o_base + j;
-    if (o >= out_dim) break;
-    const uint4* wr = reinterpret_cast<const uint4*>(W + static_cast<size_t>(o) * in_dim);
-    float a0 = 0.f, a1 = 0.f;
-    for (int c = lane; c < chunks; c += 32) {
-      const uint4 wv = wr[c];
-      const float* x0 = xs + c * 8;
-      const float* x1 = xs + in_dim + c * 8;
-      const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+  // the warp's rows side by side, so each lane has a 16-byte load of every row in
+  // flight; each row's per-lane sum runs over c in the same order as alone
+  const uint4* wr[kOutPerWarp];
+#pragma unroll
+  for (int j = 0; j < kOutPerWarp; ++j)
+    wr[j] = reinterpret_cast<const uint4*>(W + static_cast<size_t>(min(o_base + j, out_dim - 1)) * in_dim);
+  float a0[kOutPerWarp], a1[kOutPerWarp];
+#pragma unroll
+  for (int j = 0; j < kOutPerWarp; ++j) a0[j] = a1[j] = 0.f;
+  for (int c = lane; c < chunks; c += 32) {
+    uint4 wv[kOutPerWarp];
+#pragma unroll
+    for (int j = 0; j < kOutPerWarp; ++j) wv[j] = wr[j][c];
+    const float* x0 = xs + c * 8;
+    const float* x1 = xs + in_dim + c * 8;
+#pragma unroll
+    for (int j = 0; j < kOutPerWarp; ++j) {
+      const uint32_t ws[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float lo = __uint_as_float(ws[q] << 16);
         const float hi = __uint_as_float(ws[q] & 0xFFFF0000u);
-        a0 += lo * x0[2 * q] + hi * x0[2 * q + 1];
-        a1 += lo * x1[2 * q] + hi * x1[2 * q + 1];
+        a0[j] += lo * x0[2 * q] + hi * x0[2 * q + 1];
+        a1[j] += lo * x1[2 * q] + hi * x1[2 * q + 1];
       }
     }
-    a0 = warp_sum(a0);
-    a1 = warp_sum(a1);
-    if (lane == 0) {
+  }
+#pragma unroll
+  for (int j = 0; j < kOutPerWarp; ++j) {
+    const int o = o_base + j;
+    const float s0 = warp_sum(a0[j]);
+    const float s1 = warp_sum(a1[j]);
+    if (lane == 0 && o < out_dim) {
       const float bb = bf16_bits_to_float(b[o]);
-      y[o] = a0 + bb;
-      y[out_dim + o] = a1 + bb;
+      y[o] = s0 + bb;
+      y[out_dim + o] = s1 + bb;
     }
   }
 }
