@@ -14,7 +14,7 @@ Sources
   causally over text only; `proj_out` is the output head.
 * Host contract section 6: the DiT's timestep input is t = timesteps[i] / 1000.
 
-Readings where the pages leave a step open (each is listed in the design doc):
+Readings where the pages leave a step open:
 * timestep embedding: 256-wide sinusoid [cos | sin] of 1000*t with
   omega_k = 10000^(-k/128), then Linear 256->4096, SiLU, Linear 4096->4096;
 * modulation: mod = Linear(SiLU(temb)) 4096->16384, split in that order into

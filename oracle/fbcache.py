@@ -7,7 +7,7 @@ first-block cache; block 0 always runs, and blocks 1 to 31 are skipped while
 block 0's residual changes less than a threshold (the options table gives
 `--first-block-cache 0.08`; the timing table calls the mode approximate).
 
-Readings where the page is silent (each listed in the design doc):
+Readings where the page is silent:
 * "block 0's residual" is r0 = x1 - x0 on the image rows, x0 the residual stream
   entering block 0 and x1 the one leaving it (text rows are constant over a run);
 * its "change" is the relative mean absolute difference

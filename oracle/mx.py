@@ -10,7 +10,7 @@ one scale X = 2^e stored as an unbiased-by-127 byte (E8M0), and each value is
 stored as FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
 infinities, S.1111.111 is NaN, largest finite 448).
 
-Readings (each listed in the design doc):
+Readings:
 * the shared exponent follows the MX definition e = floor(log2(max |v|)) - 8
   (8 = the exponent of E4M3's largest normal), clamped to [-127, 127]; an
   all-zero block takes e = -127;
