@@ -159,6 +159,22 @@ def oracle_block_sample(samples: int, seed: int = CASE.seed):
     return times
 
 
+def step_mix(steps: int):
+    """(joint, image-only) steps among `steps` sampler steps of back-to-back 40-step images."""
+    njoint = sum(1 for i in range(steps) if i % STEPS_PER_IMAGE == 0)
+    return njoint, steps - njoint
+
+
+def arm_config(world: int, steps: int) -> dict:
+    """The workload both arms report."""
+    njoint, nimg = step_mix(steps)
+    return {"workload": "1024^2 sampler steps: N=4096 image tokens, L=407 text rows, 32 blocks, "
+                        "40-step images back to back (step 0 joint + text K/V capture, 39 image-only)",
+            "global_batch": world, "seq_len": L + N, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2: 14.2 GB of weights stream through every step",
+            "joint_steps": njoint, "image_only_steps": nimg}
+
+
 def cores_used() -> int:
     try:
         from threadpoolctl import threadpool_info
@@ -187,18 +203,21 @@ def run_reference(args, rank, world):
     nsamp = args.warmup + args.steps
     times = oracle_block_sample(nsamp)
     timed = times[args.warmup:]
-    per_step = float(np.mean(timed)) * SAMPLES_PER_STEP
+    image_step = float(np.mean(timed)) * SAMPLES_PER_STEP
+    # the same step mix as the GPU arm: a joint step costs its algorithmic FLOPs' share more
+    njoint, nimg = step_mix(args.steps)
+    per_step = image_step * (njoint * step_flops(True) + nimg * step_flops(False)) / (args.steps * step_flops(False))
     value = 1.0 / per_step
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "1024^2 image-only sampler step, N=4096, L=407, 32 blocks", "global_batch": 1,
-                   "seq_len": L + N, "parallelism": "none"},
+        "config": arm_config(world, args.steps),
         "impl": "reference",
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores_used(), "kind": "oracle",
                          "sample": f"per bench step one oracle slice (numpy fp32): 512 image rows of one "
-                                   f"block with precomputed K/V; a step is {SAMPLES_PER_STEP} slices; "
+                                   f"block with precomputed K/V; an image-only step is {SAMPLES_PER_STEP} slices, "
+                                   f"a joint step that times its algorithmic FLOPs over an image-only step's; "
                                    f"{len(timed)} timed slices"},
         "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -297,8 +316,7 @@ def run_ours(args, rank, world, local_rank):
     dit.check()
     ms = max_over_ranks(e0.elapsed_time(e1), world)
 
-    njoint = sum(1 for i in range(args.steps) if i % STEPS_PER_IMAGE == 0)
-    nimg = args.steps - njoint
+    njoint, nimg = step_mix(args.steps)
     flops = njoint * step_flops(True) + nimg * step_flops(False)
     value = world * args.steps / (ms / 1e3)
     tflops = world * flops / (ms / 1e3) / 1e12
@@ -472,11 +490,7 @@ def run_ours(args, rank, world, local_rank):
         "dtype_note": "tensor-core products on fp16 operands (the bf16 weights convert exactly) with fp32 "
                       "accumulation; fp32 residual stream, norms, modulation and softmax statistics",
         "data": "synthetic",
-        "config": {"workload": "1024^2 sampler steps: N=4096 image tokens, L=407 text rows, 32 blocks, "
-                               "40-step images back to back (step 0 joint + text K/V capture, 39 image-only)",
-                   "global_batch": world, "seq_len": L + N, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2: 14.2 GB of weights stream through every step",
-                   "joint_steps": njoint, "image_only_steps": nimg},
+        "config": arm_config(world, args.steps),
         "achieved_tflops": tflops,
         "tflops_frac_of_peak": tflops / world / peak_b,
         "tflops_frac_of_sustained_peak": tflops / world / peak_s,
@@ -517,11 +531,13 @@ def run_ours(args, rank, world, local_rank):
                 f"{BREAKDOWN_STEPS}-step pass); 1 joint + image-only"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         times = oracle_block_sample(9)
-        per_step = float(np.mean(times[1:])) * SAMPLES_PER_STEP
+        image_step = float(np.mean(times[1:])) * SAMPLES_PER_STEP
+        per_step = image_step * flops / (args.steps * step_flops(False))  # the timed steps' joint / image-only mix
         line["cpu_baseline"] = {"value": 1.0 / per_step, "unit": "steps/s", "cores": cores_used(),
                                 "kind": "oracle",
                                 "sample": f"8 timed oracle slices (numpy fp32, 512 image rows of one 1024^2 block "
-                                          f"each, K/V precomputed), scaled by {SAMPLES_PER_STEP} slices per step"}
+                                          f"each, K/V precomputed), scaled by {SAMPLES_PER_STEP} slices per "
+                                          f"image-only step and by algorithmic FLOPs to the timed steps' mix"}
     dit.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
