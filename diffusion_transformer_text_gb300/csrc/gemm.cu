@@ -40,8 +40,8 @@
 // Last wave: when the tiles left after the full waves fill at most half the
 // grid (of CTAs, or of pairs), each of them runs as two 128-column halves (the
 // MMA with N = 128 produces the same bits per element as with N = 256), so the
-// last wave takes half as long. Not for the gate/up GEMM, whose 256-column
-// tiles pair gate and up columns.
+// last wave takes half as long (the gate/up weight's 64-row interleave makes a
+// 128-column half hold matching gate and up columns).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -280,14 +280,16 @@ __device__ __forceinline__ void epi_resid(const GemmParams& p, uint32_t taddr, i
   }
 }
 
+// SwiGLU epilogue. The gate/up weight is interleaved in 64-row groups, so every
+// 128 tile columns hold the gate rows of 64 hidden units followed by their up
+// rows: block b = n0 / 128 + j of the tile yields h columns 64 b .. 64 b + 63,
+// and a 128-column half tile is a whole block.
 template <bool EARLY>
-__device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, int row, int n0,
+__device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, int row, int n0, int ncols,
                                            uint64_t* sf_bar) {
   const bool valid = row < p.M;
   const float rinv = valid ? row_rinv(p.ssp_in, row) : 0.f;
-  // tile columns [0,128) are gate rows 128j.., [128,256) the matching up rows
-  act_t* dst = p.h + static_cast<size_t>(row) * kFfn + (n0 / kBN) * (kBN / 2);
-  auto chunk = [&](int c, const uint32_t(&g)[32], const uint32_t(&u)[32]) {
+  auto chunk = [&](int j, int c, const uint32_t(&g)[32], const uint32_t(&u)[32]) {
     if (!valid) return;
     float hv[32];
 #pragma unroll
@@ -298,16 +300,16 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, 
       // below the fp16 / E4M3 rounding of h (and e^-a = inf gives -0, the limit)
       hv[i] = __fdividef(a, 1.f + __expf(-a)) * b;
     }
+    const int hcol = (n0 / 128 + j) * 64 + c * 32;
     if (p.hq) {
       // MXFP8: these 32 h columns are one block of the down GEMM's A operand
-      const int hcol = (n0 / kBN) * (kBN / 2) + c * 32;
       p.hsf[mx_sf_offset(row, hcol / 32, (p.M + kBM - 1) / kBM)] =
           mx_quant32(hv, p.hq + static_cast<size_t>(row) * kFfn + hcol);
     } else {
-      store_f16x32(dst + c * 32, hv);
+      store_f16x32(p.h + static_cast<size_t>(row) * kFfn + hcol, hv);
     }
   };
-  int c0 = 0;
+  int j0 = 0;
   if (EARLY) {
     // MXFP8: gate columns 0..63 hold the next tile's scale sets once released
     uint32_t g0[32], g1[32];
@@ -317,26 +319,29 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams& p, uint32_t taddr, 
     release_sf_now(sf_bar);
     {
       uint32_t u[32];
-      tmem_ld32(taddr + kBN / 2, u);
+      tmem_ld32(taddr + 64, u);
       tmem_ld_wait();
-      chunk(0, g0, u);
+      chunk(0, 0, g0, u);
     }
     {
       uint32_t u[32];
-      tmem_ld32(taddr + kBN / 2 + 32, u);
+      tmem_ld32(taddr + 96, u);
       tmem_ld_wait();
-      chunk(1, g1, u);
+      chunk(0, 1, g1, u);
     }
-    c0 = 2;
+    j0 = 1;
   }
 #pragma unroll 1
-  for (int c = c0; c < kBN / 64; ++c) {
-    uint32_t g[32], u[32];
-    tmem_ld32(taddr + c * 32, g);
-    tmem_ld32(taddr + kBN / 2 + c * 32, u);
-    tmem_ld_wait();
-    if (!EARLY) release_sf_cols(sf_bar, c);
-    chunk(c, g, u);
+  for (int j = j0; j < ncols / 128; ++j) {
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {
+      uint32_t g[32], u[32];
+      tmem_ld32(taddr + j * 128 + c * 32, g);
+      tmem_ld32(taddr + j * 128 + 64 + c * 32, u);
+      tmem_ld_wait();
+      if (!EARLY) release_sf_cols(sf_bar, 2 * j + c);
+      chunk(j, c, g, u);
+    }
   }
 }
 
@@ -561,7 +566,7 @@ __global__ void __launch_bounds__(192, 1)
         epi_resid(p, taddr, mt * kBM + quarter * 32, lane, n0, ncols,
                   reinterpret_cast<float*>(smem + kMxStages * G::kStage + 256) + (warp - 2) * 32 * 33, sf_bar);
       else if (KIND == kEpiSwiglu)
-        epi_swiglu<true>(p, taddr, row, nt * kBN, sf_bar);  // never split: a tile pairs gate and up columns
+        epi_swiglu<true>(p, taddr, row, n0, ncols, sf_bar);
       else
         epi_f32(p, taddr, row, n0, ncols, sf_bar);
       tc_fence_before();
@@ -782,7 +787,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         epi_resid(p, taddr, row - lane, lane, n0, ncols,
                   reinterpret_cast<float*>(smem + kPairStages * kPairStage + 256) + (warp - 2) * 32 * 33, nullptr);
       else if (KIND == kEpiSwiglu)
-        epi_swiglu<false>(p, taddr, row, nt * kBN, nullptr);  // never split: a tile pairs gate and up columns
+        epi_swiglu<false>(p, taddr, row, n0, ncols, nullptr);
       else
         epi_f32(p, taddr, row, n0, ncols, nullptr);
       tc_fence_before();
@@ -837,7 +842,7 @@ cudaError_t launch_pair_any(EpiKind kind, const CUtensorMap& a, const CUtensorMa
   GemmParams q = p;
   q.tail_start = tiles;
   const int rem = tiles % clusters;
-  if (kind != kEpiSwiglu && rem > 0 && 2 * rem <= clusters) q.tail_start = tiles - rem;
+  if (rem > 0 && 2 * rem <= clusters) q.tail_start = tiles - rem;
   const int units = q.tail_start + 2 * (tiles - q.tail_start);
   const int grid = 2 * (units < clusters ? units : clusters);
   switch (kind) {
@@ -875,7 +880,7 @@ cudaError_t launch_mx_any(EpiKind kind, const CUtensorMap& a, const CUtensorMap&
   GemmParams q = p;
   q.tail_start = tiles;
   const int rem = tiles % grid_ctas;
-  if (kind != kEpiSwiglu && rem > 0 && 2 * rem <= grid_ctas) q.tail_start = tiles - rem;
+  if (rem > 0 && 2 * rem <= grid_ctas) q.tail_start = tiles - rem;
   const int units = q.tail_start + 2 * (tiles - q.tail_start);
   const int grid = units < grid_ctas ? units : grid_ctas;
   switch (kind) {

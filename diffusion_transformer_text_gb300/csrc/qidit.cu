@@ -136,7 +136,7 @@ struct qi_dit {
   struct Block {
     uint16_t* wqkv;  // [3*4096, 4096]: Q rows, K rows, V rows
     uint16_t* wo;    // [4096, 4096]
-    uint16_t* wgu;   // [2*12288, 4096]: per 128-row group j, gate rows then up rows
+    uint16_t* wgu;   // [2*12288, 4096]: per 64-row group j, gate rows then up rows
     uint16_t* wd;    // [4096, 12288]
     CUtensorMap m_qkv, m_o, m_gu, m_d;
   };
@@ -841,11 +841,12 @@ qi_status qi_dit_load_block(qi_dit* d, int block, const qi_block_weights* w, int
   QI_CUDA(cudaMemcpyAsync(B.wqkv + sq, w->wk, sq * 2, kind, s));
   QI_CUDA(cudaMemcpyAsync(B.wqkv + 2 * sq, w->wv, sq * 2, kind, s));
   QI_CUDA(cudaMemcpyAsync(B.wo, w->wo, sq * 2, kind, s));
-  // gate/up interleave: 128-row groups, gate group j then up group j
-  const size_t grp = (size_t)(kBN / 2) * kHidden * 2;  // bytes per 128-row group
-  QI_CUDA(cudaMemcpy2DAsync(B.wgu, 2 * grp, w->wg, grp, grp, kFfn / (kBN / 2), kind, s));
-  QI_CUDA(cudaMemcpy2DAsync(reinterpret_cast<char*>(B.wgu) + grp, 2 * grp, w->wu, grp, grp, kFfn / (kBN / 2), kind,
-                            s));
+  // gate/up interleave: 64-row groups, gate group j then up group j, so any 128
+  // GEMM columns (a half tile) pair the gate and up rows of the same 64 hidden units
+  constexpr int kGuRows = 64;
+  const size_t grp = (size_t)kGuRows * kHidden * 2;  // bytes per 64-row group
+  QI_CUDA(cudaMemcpy2DAsync(B.wgu, 2 * grp, w->wg, grp, grp, kFfn / kGuRows, kind, s));
+  QI_CUDA(cudaMemcpy2DAsync(reinterpret_cast<char*>(B.wgu) + grp, 2 * grp, w->wu, grp, grp, kFfn / kGuRows, kind, s));
   QI_CUDA(cudaMemcpyAsync(B.wd, w->wd, (size_t)kHidden * kFfn * 2, kind, s));
   if (d->has_mx) {
     // from the bf16 values themselves, before they become fp16

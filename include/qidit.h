@@ -156,7 +156,7 @@ qi_status qi_dit_load_global(qi_dit* dit, const qi_global_weights* w, int src_on
                              qi_stream_t stream);
 
 /* Copy block `block`'s matrices into the handle (repacked internally: Q|K|V
- * stacked, gate/up interleaved by 128-row groups). Returns after completion. */
+ * stacked, gate/up interleaved by 64-row groups). Returns after completion. */
 qi_status qi_dit_load_block(qi_dit* dit, int block, const qi_block_weights* w,
                             int src_on_device, qi_stream_t stream);
 
