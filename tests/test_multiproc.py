@@ -63,3 +63,19 @@ def test_reference_arm_prints_on_rank_0_only():
     assert outs[0] == ""
     line = json.loads(outs[1].splitlines()[-1])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    # the same workload description as the GPU arm's line
+    sys.path.insert(0, ROOT)
+    import bench
+    assert line["config"] == bench.arm_config(2, 1)
+    assert line["e2e"]["value"] == line["value"] and line["cpu_baseline"]["value"] == line["value"]
+
+
+def test_step_mix():
+    """Back-to-back 40-step images: step 0 of each image is the joint pass."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.step_mix(40) == (1, 39)
+    assert bench.step_mix(41) == (2, 39)
+    assert bench.step_mix(1) == (1, 0)
+    cfg = bench.arm_config(4, 80)
+    assert cfg["joint_steps"] == 2 and cfg["image_only_steps"] == 78 and cfg["global_batch"] == 4
