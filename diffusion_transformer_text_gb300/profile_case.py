@@ -3,8 +3,9 @@
     python -m diffusion_transformer_text_gb300.profile_case [--blocks 2] [--steps 2] [--N 4096] [--L 407] [--mxfp8]
 
 Builds a handle with `blocks` blocks of random-init bf16 weights drawn on the
-device, runs one joint step (text K/V capture) and then `steps` image-only
-steps at N image tokens and L text rows, and prints the wall time. With two
+device, packs a noise latent, runs one joint step (text K/V capture) and then
+`steps` image-only steps at N image tokens and L text rows, each followed by the
+Euler update, and prints the wall time. With two
 blocks it holds about 1.5 GB on the device (weights alone exceed the L2), so a
 full profiler capture of one launch stays small. Launch order per pass: text
 GEMM (joint only), then per block QKV GEMM, attention, out-projection GEMM,
@@ -50,13 +51,15 @@ def main():
     d.set_mxfp8(a.mxfp8)
     tc, ts, ic, is_ = qi.rope_tables(a.L, h, w)
     txt = torch.randn(a.L, 4096, generator=g, device=dev)
-    x = torch.randn(a.N, 64, generator=g, device=dev)
+    x = qi.pack_noise(torch.randn(64, h, w, generator=g, device=dev))
     sig, tsteps = qi.flow_sigmas(40, a.N)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     vel = d.step(x, txt, float(np.float32(tsteps[0]) / np.float32(1000)), tc, ts, ic, is_)
+    qi.euler_update(x, vel, float(sig[0]), float(sig[1]))
     for i in range(1, a.steps + 1):
         vel = d.step_cached(x, a.L, float(np.float32(tsteps[i]) / np.float32(1000)), ic, is_, vel=vel)
+        qi.euler_update(x, vel, float(sig[i]), float(sig[i + 1]))
     torch.cuda.synchronize()
     d.check()
     print(f"profile case: blocks {a.blocks}, N {a.N}, L {a.L}, mxfp8 {a.mxfp8}, 1 joint + {a.steps} image-only steps, "
