@@ -7,10 +7,21 @@ Euler update. K timed steps run images back to back from step 0.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Prints one JSON line (rank 0). Under torchrun each rank runs an independent
-replica on its own GPU (the step has no exchange between images): weak scaling.
-The reference arm times the CPU oracle on this host's cores on a bounded sample
-(per bench step, 512 image rows of one 1024^2 block; 256 such slices make a step).
+Prints one JSON line (rank 0). Besides the headline it carries:
+* `configs`: the other workloads (one block at 128^2; 256^2; 384^2 with a 22- and a
+  494-token prompt, joint and cached steps; 2048^2 joint and cached) with steps/s,
+  tokens/s, algorithmic TFLOP/s and their fractions of the measured peaks, the
+  median SM clock of each run and, where the oracle finishes in seconds, the
+  oracle's whole step timed on the host cores;
+* `kernel_classes`: each kernel class's time per step, TFLOP/s and fraction of the
+  peak, also at equal clock (the peak's measured clock);
+* `e2e`: the sampler step through the C ABI with host buffers
+  (qi_dit_euler_step with QI_STEP_HOST_IO: copies in, DiT pass, Euler update,
+  copy of x out and a stream synchronisation in every call).
+Under torchrun each rank runs an independent replica on its own GPU (the step has
+no exchange between images): weak scaling. The reference arm times the CPU oracle
+on this host's cores on a bounded sample (per bench step, 512 image rows of one
+1024^2 block; 256 such slices make a step).
 """
 from __future__ import annotations
 
@@ -39,14 +50,34 @@ L = CASE.L
 HIDDEN, FFN, BLOCKS = 4096, 12288, 32
 GU_STRIDE = 4                              # gate/up GEMM timed in blocks 0, 4, 8, ...
 GU_BLOCKS = len(range(0, BLOCKS, GU_STRIDE))
+BLOCK_PARAMS = 4 * HIDDEN * HIDDEN + 3 * HIDDEN * FFN
+# HBM bytes a pass must read however it is tiled: the fp16 block weights, the
+# timestep MLP's second matrix and the shared modulation weight (bf16), and on a
+# joint pass the text projection (fp16)
+WEIGHT_BYTES_BLOCK = 2 * BLOCK_PARAMS
+MOD_BYTES = 2 * (HIDDEN * HIDDEN + 4 * HIDDEN * HIDDEN)
+TXT_W_BYTES = 2 * HIDDEN * HIDDEN
+
+
+def pass_flops(Lq: int, Nq: int, joint: bool, blocks: int = BLOCKS) -> int:
+    """Algorithmic FLOPs of one DiT pass (GEMMs + attention), as in the oracle's accounting."""
+    R = Lq + Nq if joint else Nq
+    gemm = 2 * R * BLOCK_PARAMS
+    att = Nq * (Nq + Lq) * 4 * HIDDEN + (Lq * (Lq + 1) // 2 * 4 * HIDDEN if joint else 0)
+    return blocks * (gemm + att)
 
 
 def step_flops(joint: bool) -> int:
-    """Algorithmic FLOPs of one DiT pass (GEMMs + attention), as in the oracle's accounting."""
-    R = L + N if joint else N
-    gemm = 2 * R * (4 * HIDDEN * HIDDEN + 3 * HIDDEN * FFN)
-    att = N * (N + L) * 4 * HIDDEN + (L * (L + 1) // 2 * 4 * HIDDEN if joint else 0)
-    return BLOCKS * (gemm + att)
+    return pass_flops(L, N, joint)
+
+
+def class_flops(Lq: int, Nq: int, joint: bool) -> dict:
+    """Algorithmic FLOPs of each block kernel class over one pass (all blocks)."""
+    R = Lq + Nq if joint else Nq
+    att = Nq * (Nq + Lq) * 4 * HIDDEN + (Lq * (Lq + 1) // 2 * 4 * HIDDEN if joint else 0)
+    per_block = {"qkv_gemm": 2 * R * HIDDEN * 3 * HIDDEN, "attention": att, "out_gemm": 2 * R * HIDDEN * HIDDEN,
+                 "gateup_gemm": 2 * R * HIDDEN * 2 * FFN, "down_gemm": 2 * R * FFN * HIDDEN}
+    return {k: BLOCKS * v for k, v in per_block.items()}
 
 
 def gateup_flops(joint: bool) -> int:
@@ -61,12 +92,21 @@ def launches_per_step(joint: bool) -> int:
 
 
 def peaks():
+    """(bf16 burst TFLOP/s, bf16 sustained TFLOP/s, HBM GB/s, SM MHz the peaks ran at, 'measured'|'fallback')."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return p["bf16_tflops"], p.get("bf16_tflops_sustained"), p["hbm_gbs"], "measured"
+        mhz = (p.get("clocks_under_load") or {}).get("sm_mhz_median")
+        return p["bf16_tflops"], p.get("bf16_tflops_sustained"), p["hbm_gbs"], mhz, "measured"
     except Exception:
-        return 1900.0, 1700.0, 6800.0, "fallback"
+        return 1900.0, 1700.0, 6800.0, None, "fallback"
+
+
+def frac_at_clock(achieved: float, mhz, peak: float, peak_mhz):
+    """achieved / peak with both taken per MHz of the SM clock they ran at (None if a clock is unknown)."""
+    if not achieved or not mhz or not peak_mhz:
+        return None
+    return (achieved / mhz) / (peak / peak_mhz)
 
 
 class Clocks:
@@ -76,7 +116,7 @@ class Clocks:
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu: int):
+    def __init__(self, gpu):
         self.gpu = gpu
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         self.p = None
@@ -88,6 +128,7 @@ class Clocks:
                                       stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.p = None
+        return self
 
     def stop(self):
         if self.p is None:
@@ -157,6 +198,52 @@ def oracle_block_sample(samples: int, seed: int = CASE.seed):
         odit.block_after_attention(bw, x[rows], o, g1[rows], s2[rows], g2[rows])
         times.append(time.perf_counter() - t0)
     return times
+
+
+def oracle_whole_steps():
+    """Whole oracle calls on the workloads where one finishes in seconds on the host cores:
+    the one-block case (modulation rows and the block), the 256^2 step and the 384^2 joint
+    step with the 22-token prompt (dense joint passes over all 32 blocks). Returns
+    {config: {"s_per_step", "steps_per_s", "tflops", "reps"}}."""
+    from oracle import dit as odit
+    from oracle import rope as orope
+    out = {}
+    # one block (128^2, L = 8): modulation for t = 0.5 and t = 0, then the block
+    bc = synth.BLOCK_CASE
+    Wb = synth.Weights(seed=bc.seed, nblocks=1)
+    bw = Wb.block(0)
+    xb = synth.block_hidden(bc)
+    tc, ts, ic, is_ = orope.token_tables(bc.L, bc.h, bc.w)
+    cos, sin = np.concatenate([tc, ic]), np.concatenate([ts, is_])
+
+    def one_block():
+        mods = odit.row_mods(odit.modulation(Wb.glob, np.float32(bc.timestep)), odit.modulation(Wb.glob, 0.0),
+                             bc.L, bc.L + bc.N)
+        odit.block_forward(bw, xb, mods, bc.L, cos, sin, 32)
+
+    one_block()
+    reps, t0 = 3, time.perf_counter()
+    for _ in range(reps):
+        one_block()
+    dt = (time.perf_counter() - t0) / reps
+    out["block_128"] = {"s_per_step": dt, "steps_per_s": 1 / dt, "reps": reps,
+                        "tflops": pass_flops(bc.L, bc.N, True, blocks=1) / dt / 1e12}
+    del Wb, bw
+    # 32 blocks: one weight set (256^2 seed) drawn before timing and used for both shapes
+    W = synth.Weights(seed=synth.STEP_256.seed)
+    for b in range(W.nblocks):
+        W.block(b)
+    for key, case in (("step_256", synth.STEP_256), ("step_384_L22", synth.STEP_384_L22)):
+        img = synth.img_tokens(case)
+        txt = synth.txt_feats(case)
+        tabs = orope.token_tables(case.L, case.h, case.w)
+        t = np.float32(case.timestep if case.timestep is not None else 0.97)
+        t0 = time.perf_counter()
+        odit.dit_forward(W, img, txt, t, *tabs)
+        dt = time.perf_counter() - t0
+        out[key] = {"s_per_step": dt, "steps_per_s": 1 / dt, "reps": 1,
+                    "tflops": pass_flops(case.L, case.N, True) / dt / 1e12}
+    return out
 
 
 def step_mix(steps: int):
@@ -244,6 +331,114 @@ def gpu_weights(dit, seed, device):
     torch.cuda.synchronize()
 
 
+def time_repeated(fn, stream, gpu_id, target_s: float = 1.0, min_reps: int = 5, max_reps: int = 5000):
+    """CUDA-event time of `fn` (one unit of work) repeated for about target_s seconds,
+    after two untimed calls; nvidia-smi clocks sampled during the repetitions.
+    Returns (ms per call, reps, clocks)."""
+    import torch
+    fn()
+    fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    est = max(a.elapsed_time(b) / 1e3, 1e-6)
+    reps = int(min(max_reps, max(min_reps, target_s / est)))
+    clk = Clocks(gpu_id).start()
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps, reps, clk.stop()
+
+
+def config_entry(ms: float, rows: int, flops: int, hbm_bytes: int, clk, pk) -> dict:
+    """steps/s, tokens/s and the fractions of the measured peaks for one timed unit of work."""
+    peak_b, peak_s, hbm, peak_mhz, _ = pk
+    tflops = flops / (ms / 1e3) / 1e12
+    floor_compute_ms = flops / (peak_b * 1e12) * 1e3
+    floor_hbm_ms = hbm_bytes / (hbm * 1e9) * 1e3
+    mhz = clk.get("sm_mhz") if clk else None
+    return {"ms_per_step": ms, "steps_per_s": 1e3 / ms, "tokens_per_s": rows / (ms / 1e3),
+            "tflops": tflops, "tflop_per_step": flops / 1e12,
+            "frac_of_burst": tflops / peak_b, "frac_of_sustained": tflops / peak_s,
+            "frac_clock_normalised": frac_at_clock(tflops, mhz, peak_s, peak_mhz),
+            "floor_ms": {"compute": floor_compute_ms, "hbm": floor_hbm_ms},
+            "bound": "tensor" if floor_compute_ms >= floor_hbm_ms else "hbm",
+            "frac_of_floor": max(floor_compute_ms, floor_hbm_ms) / ms,
+            "clocks": clk}
+
+
+def bench_configs(qi, dit, stream, gpu_id, pk) -> dict:
+    """The other workloads on the same handle and weights (one random-init set)."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device=dev)
+    g.manual_seed(77)
+    out = {}
+
+    # one block at 128^2 (L = 8, 8x8 grid, t = 0.5 for image rows): the test-hook call that
+    # computes the two modulation rows and runs block 0 in place on hidden [72, 4096]
+    bc = synth.BLOCK_CASE
+    hid0 = torch.randn(bc.L + bc.N, HIDDEN, generator=g, device=dev)
+    hid = hid0.clone()
+    tc, ts, ic, is_ = qi.rope_tables(bc.L, bc.h, bc.w)
+    cos, sin = torch.cat([tc, ic]).contiguous(), torch.cat([ts, is_]).contiguous()
+
+    def one_block():
+        hid.copy_(hid0)  # the block updates hidden in place: every call starts from the same input
+        dit.block_forward(0, hid, bc.L, bc.timestep, cos, sin)
+
+    ms, reps, clk = time_repeated(one_block, stream, gpu_id)
+    dit.check()
+    e = config_entry(ms, bc.L + bc.N, pass_flops(bc.L, bc.N, True, blocks=1), WEIGHT_BYTES_BLOCK + MOD_BYTES, clk, pk)
+    e.update({"reps": reps, "shape": "hidden [72, 4096]: L=8 text rows + 8x8 image grid, block 0 + modulation rows "
+                                     "(each call also restores the 1.2 MB input)",
+              "hbm_bytes_note": "fp16 block weights (436 MB) + timestep MLP and modulation weights (168 MB)"})
+    out["block_128"] = e
+
+    def joint_and_cached(case, t, n_cached: bool):
+        Lc, hc, wc = case.L, case.h, case.w
+        Nc = hc * wc
+        img = torch.randn(Nc, 64, generator=g, device=dev)
+        txt = torch.randn(Lc, HIDDEN, generator=g, device=dev)
+        tc_, ts_, ic_, is__ = qi.rope_tables(Lc, hc, wc)
+        vel = torch.empty(Nc, 64, device=dev)
+        res = {}
+        ms_j, reps_j, clk_j = time_repeated(lambda: dit.step(img, txt, t, tc_, ts_, ic_, is__, vel=vel), stream,
+                                            gpu_id, min_reps=3)
+        dit.check()
+        res["joint"] = config_entry(ms_j, Lc + Nc, pass_flops(Lc, Nc, True),
+                                    BLOCKS * WEIGHT_BYTES_BLOCK + MOD_BYTES + TXT_W_BYTES, clk_j, pk)
+        res["joint"]["reps"] = reps_j
+        if n_cached:
+            ms_c, reps_c, clk_c = time_repeated(lambda: dit.step_cached(img, Lc, t, ic_, is__, vel=vel), stream,
+                                                gpu_id, min_reps=3)
+            dit.check()
+            res["cached"] = config_entry(ms_c, Nc, pass_flops(Lc, Nc, False), BLOCKS * WEIGHT_BYTES_BLOCK + MOD_BYTES,
+                                         clk_c, pk)
+            res["cached"]["reps"] = reps_c
+            # the pages' five-step run at this size: step 1 joint + capture, steps 2-5 cached
+            five = ms_j + 4 * ms_c
+            res["five_steps"] = {"ms": five, "steps_per_s": 5e3 / five,
+                                 "tflops": (pass_flops(Lc, Nc, True) + 4 * pass_flops(Lc, Nc, False)) / (five / 1e3)
+                                 / 1e12}
+        return res
+
+    out["step_256"] = joint_and_cached(synth.STEP_256, synth.STEP_256.timestep, False)["joint"]
+    out["step_256"]["shape"] = "N=256 (16x16), L=22, t=0.97, joint pass"
+    for key, case in (("step_384_L22", synth.STEP_384_L22), ("step_384_L494", synth.STEP_384_L494)):
+        out[key] = joint_and_cached(case, 0.97, True)
+        out[key]["shape"] = f"N=576 (24x24), L={case.L}: joint (+capture) and cached image-only steps"
+    out["step_2048"] = joint_and_cached(synth.STEP_2048, 0.97, True)
+    out["step_2048"]["shape"] = "N=16384 (128x128), L=512: joint (+capture) and cached image-only steps"
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -254,8 +449,11 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     qi.build()
     stream = torch.cuda.current_stream()
+    pk = peaks()
+    peak_b, peak_s, hbm, peak_mhz, peak_kind = pk
 
-    dit = qi.DiT(blocks=BLOCKS, L_max=L, N_max=N, device=local_rank, kv_slots=2, mxfp8=True)
+    # one handle for every workload: L up to 512, N up to 16384 (2048^2), two K/V slots, MXFP8 copies
+    dit = qi.DiT(blocks=BLOCKS, L_max=512, N_max=16384, device=local_rank, kv_slots=2, mxfp8=True)
     gpu_weights(dit, CASE.seed * 1000 + rank, dev)
 
     sig, ts = qi.flow_sigmas(STEPS_PER_IMAGE, N)
@@ -315,6 +513,7 @@ def run_ours(args, rank, world, local_rank):
     dit.profile(False)
     dit.check()
     ms = max_over_ranks(e0.elapsed_time(e1), world)
+    mhz = clk.get("sm_mhz") if clk else None
 
     njoint, nimg = step_mix(args.steps)
     flops = njoint * step_flops(True) + nimg * step_flops(False)
@@ -337,6 +536,16 @@ def run_ours(args, rank, world, local_rank):
         return {k: v[0] / BREAKDOWN_STEPS for k, v in kp.items()}
 
     kernel_ms = breakdown()
+    cf_j, cf_i = class_flops(L, N, True), class_flops(L, N, False)
+    kernel_classes = {}
+    for k, v in kernel_ms.items():
+        ent = {"ms_per_step": v}
+        if k in cf_j and v > 0:
+            fl = (cf_j[k] + (BREAKDOWN_STEPS - 1) * cf_i[k]) / BREAKDOWN_STEPS
+            tf = fl / (v / 1e3) / 1e12
+            ent.update({"tflops": tf, "frac_of_sustained": tf / peak_s, "frac_of_burst": tf / peak_b,
+                        "frac_clock_normalised": frac_at_clock(tf, mhz, peak_s, peak_mhz)})
+        kernel_classes[k] = ent
 
     # ---- classifier-free guidance (second K/V slot): a 9-token negative prompt (the
     # host contract's empty-prompt template), guidance 2.5; 1 joint + CFG_STEPS - 1 cached
@@ -418,6 +627,7 @@ def run_ours(args, rank, world, local_rank):
     m1 = torch.cuda.Event(enable_timing=True)
     x.copy_(x0)
     dit.profile(True, classes=["gateup_gemm"], block_stride=GU_STRIDE)
+    mclk = Clocks(gpu_id).start()
     m0.record(stream)
     for i in range(MX_STEPS):
         if i == 0:
@@ -427,6 +637,7 @@ def run_ours(args, rank, world, local_rank):
         qi.euler_update(x, vel, float(sig[i]), float(sig[i + 1]))
     m1.record(stream)
     torch.cuda.synchronize()
+    mx_clk = mclk.stop()
     mx_prof = dit.profile_read()
     dit.profile(False)
     dit.check()
@@ -437,41 +648,41 @@ def run_ours(args, rank, world, local_rank):
     mx_gu_ms, _ = mx_prof["gateup_gemm"]
     mx_gu_flops = GU_BLOCKS * (gateup_flops(True) + (MX_STEPS - 1) * gateup_flops(False))
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the C ABI with host buffers: qi_dit_euler_step with
+    # QI_STEP_HOST_IO copies x and the tables (and, on a joint step, the prompt) in from
+    # pinned memory, runs the DiT pass and the Euler update, copies x back and
+    # synchronises, in every call
     xh = torch.empty(N, 64, dtype=torch.float32).pin_memory()
-    xh.copy_(x0.cpu())
     txth = txt.cpu().pin_memory()
     tabs_h = [t.cpu().pin_memory() for t in (tc, tsn, ic, isn)]
-    txt_d = torch.empty_like(txt)
-    tabs_d = [torch.empty_like(t) for t in (tc, tsn, ic, isn)]
+    x0h = x0.cpu()
 
     def e2e_step(i):
         k = i % STEPS_PER_IMAGE
-        x.copy_(xh, non_blocking=True)
         if k == 0:
-            txt_d.copy_(txth, non_blocking=True)
-            for d_, h_ in zip(tabs_d, tabs_h):
-                d_.copy_(h_, non_blocking=True)
-            dit.step(x, txt_d, tvals[0], *tabs_d, vel=vel)
+            xh.copy_(x0h)
+            dit.euler_step_host(xh, txth, L, tvals[0], float(sig[0]), float(sig[1]), *tabs_h)
         else:
-            tabs_d[2].copy_(tabs_h[2], non_blocking=True)
-            tabs_d[3].copy_(tabs_h[3], non_blocking=True)
-            dit.step_cached(x, L, tvals[k], tabs_d[2], tabs_d[3], vel=vel)
-        qi.euler_update(x, vel, float(sig[k]), float(sig[k + 1]))
-        xh.copy_(x, non_blocking=True)
+            dit.euler_step_host(xh, None, L, tvals[k], float(sig[k]), float(sig[k + 1]), None, None, tabs_h[2],
+                                tabs_h[3], use_cache=True)
 
     e2e_steps = args.steps
+    for i in range(2):
+        e2e_step(i)
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(e2e_steps):
         e2e_step(i)
-    torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    dit.check()
     h2d = (N * 64 * 4 + 2 * N * 64 * 4) * e2e_steps + njoint * (L * HIDDEN * 4 + 2 * L * 64 * 4)
     d2h = N * 64 * 4 * e2e_steps
 
-    peak_b, peak_s, hbm, peak_kind = peaks()
+    # ---- the other workloads
+    configs = bench_configs(qi, dit, stream, gpu_id, pk)
+    configs["loop_1024"] = "the headline (value, roofline, kernel_classes, e2e)"
+
     gu_ms, gu_n = prof["gateup_gemm"]
     gu_flops = GU_BLOCKS * (njoint * gateup_flops(True) + nimg * gateup_flops(False))
     gu_tflops = gu_flops / (gu_ms / 1e3) / 1e12 if gu_ms > 0 else None
@@ -491,22 +702,32 @@ def run_ours(args, rank, world, local_rank):
                       "accumulation; fp32 residual stream, norms, modulation and softmax statistics",
         "data": "synthetic",
         "config": arm_config(world, args.steps),
+        "tokens_per_s": world * (njoint * (L + N) + nimg * N) / (ms / 1e3),
         "achieved_tflops": tflops,
         "tflops_frac_of_peak": tflops / world / peak_b,
         "tflops_frac_of_sustained_peak": tflops / world / peak_s,
+        "tflops_frac_clock_normalised": frac_at_clock(tflops / world, mhz, peak_s, peak_mhz),
         "gpu_launches": njoint * launches_per_step(True) + nimg * launches_per_step(False),
         "roofline": {"kernel": "gate/up GEMM + SwiGLU epilogue (tcgen05)", "bound": "tensor",
                      "achieved": gu_tflops, "peak": peak_s, "unit": "TFLOP/s",
                      "frac": (gu_tflops / peak_s) if gu_tflops else None, "traffic": traffic,
                      "peak_kind": f"{peak_kind} bf16 sustained (the kernel runs inside a seconds-long loop)",
-                     "frac_of_burst": (gu_tflops / peak_b) if gu_tflops else None, "launches": gu_n,
-                     "avg_launch_ms": gu_ms / gu_n if gu_n else None},
+                     "frac_of_burst": (gu_tflops / peak_b) if gu_tflops else None,
+                     "frac_clock_normalised": frac_at_clock(gu_tflops, mhz, peak_s, peak_mhz),
+                     "clock_mhz": mhz, "peak_clock_mhz": peak_mhz,
+                     "launches": gu_n, "avg_launch_ms": gu_ms / gu_n if gu_n else None},
         "kernel_ms_per_step": kernel_ms,
+        "kernel_classes": kernel_classes,
         "kernel_ms_note": f"separate {BREAKDOWN_STEPS}-step pass (1 joint + image-only) with every kernel class "
-                          "timed by CUDA events; the timed steps above carry events around the gate/up GEMM only",
+                          "timed by CUDA events; the timed steps above carry events around the gate/up GEMM only; "
+                          "frac_clock_normalised = (TFLOP/s / headline median SM MHz) / (sustained peak / the "
+                          "peak's median SM MHz)",
         "e2e": {"value": world * e2e_steps / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": h2d / e2e_steps,
-                "d2h_bytes_per_step": d2h / e2e_steps},
+                "d2h_bytes_per_step": d2h / e2e_steps,
+                "call": "qi_dit_euler_step(QI_STEP_HOST_IO[|QI_STEP_USE_CACHE]) on pinned host buffers: "
+                        "copies in, DiT pass, Euler update, x copied out, stream synchronised, every step"},
         "clocks": clk,
+        "configs": configs,
         "cfg": {"steps_per_s": world * 1e3 / cfg_ms, "ms_per_step": cfg_ms, "guidance": GUIDE, "neg_tokens": L_NEG,
                 "steps": CFG_STEPS, "note": "step 0: two joint passes (each prompt captures its K/V slot); "
                                             f"{CFG_STEPS - 1} image-only steps: one pass of 2N rows (batch 2)"},
@@ -520,11 +741,16 @@ def run_ours(args, rank, world, local_rank):
                             "call that skips blocks 1..31 (same input again)"},
     }
     fp8_peak = 2.0 * peak_b  # the recipe's nominal fp8 / bf16 ratio (4.5 / 2.25) on the measured bf16 burst
+    mx_mhz = mx_clk.get("sm_mhz") if mx_clk else None
+    mx_tflops = mx_flops / (mx_ms / 1e3) / 1e12
+    mx_gu = mx_gu_flops / (mx_gu_ms / 1e3) / 1e12 if mx_gu_ms > 0 else None
     line["mxfp8"] = {
         "steps_per_s": world * 1e3 / mx_ms, "ms_per_step": mx_ms, "steps": MX_STEPS,
-        "achieved_tflops": mx_flops / (mx_ms / 1e3) / 1e12,
-        "gateup_tflops": mx_gu_flops / (mx_gu_ms / 1e3) / 1e12 if mx_gu_ms > 0 else None,
+        "achieved_tflops": mx_tflops, "frac_of_fp8_peak": mx_tflops / fp8_peak,
+        "gateup_tflops": mx_gu, "gateup_frac_of_fp8_peak": mx_gu / fp8_peak if mx_gu else None,
+        "gateup_frac_clock_normalised": frac_at_clock(mx_gu, mx_mhz, 2.0 * peak_s, peak_mhz),
         "fp8_peak_tflops": fp8_peak, "peak_kind": f"{peak_kind} bf16 burst x 2 (nominal fp8/bf16 ratio)",
+        "clocks": mx_clk,
         "kernel_ms_per_step": mx_kernel_ms,
         "note": "block GEMMs on MXFP8 (E4M3, UE8M0 scale per 32); activations quantised by a separate "
                 "kernel before each GEMM (inside the GEMM classes of kernel_ms_per_step, measured in a separate "
@@ -538,6 +764,14 @@ def run_ours(args, rank, world, local_rank):
                                 "sample": f"8 timed oracle slices (numpy fp32, 512 image rows of one 1024^2 block "
                                           f"each, K/V precomputed), scaled by {SAMPLES_PER_STEP} slices per "
                                           f"image-only step and by algorithmic FLOPs to the timed steps' mix"}
+        whole = oracle_whole_steps()
+        for key, v in whole.items():
+            v["cores"] = cores_used()
+            v["what"] = ("whole oracle call (numpy fp32, dense joint pass) on the host cores"
+                         + ("; weights of the 256^2 seed" if key == "step_384_L22" else ""))
+            tgt = configs[key]["joint"] if "joint" in configs[key] else configs[key]
+            tgt["oracle"] = v
+            tgt["gpu_over_oracle"] = v["s_per_step"] * 1e3 / tgt["ms_per_step"]
     dit.close()
     if rank == 0:
         print(json.dumps(line), flush=True)

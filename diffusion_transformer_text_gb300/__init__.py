@@ -40,7 +40,7 @@ SYMBOLS = (
     "qi_dit_block_forward", "qi_dit_read_kv", "qi_dit_set_trace", "qi_dit_profile", "qi_dit_profile_classes",
     "qi_dit_profile_read", "qi_last_error", "qi_gemm_bf16", "qi_attention_f16", "qi_gemm_bf16_noalloc",
     "qi_dit_step_cfg", "qi_dpmpp2m_coeffs", "qi_dpmpp2m_update", "qi_dit_step_fbcache", "qi_dit_fbcache_reset",
-    "qi_dit_set_mxfp8", "qi_quant_mxfp8", "qi_gemm_mxfp8", "qi_debug_inject",
+    "qi_dit_set_mxfp8", "qi_quant_mxfp8", "qi_gemm_mxfp8", "qi_debug_inject", "qi_dit_euler_step",
 )
 
 
@@ -97,6 +97,7 @@ def lib() -> ctypes.CDLL:
         "qi_pack_noise": [P, I, I, P, P],
         "qi_euler_update": [P, P, I, F, F, P],
         "qi_dit_step": [P, P, I, P, I, F, P, P, P, P, P, U, P],
+        "qi_dit_euler_step": [P, P, I, P, I, F, F, F, P, P, P, P, P, U, P],
         "qi_text_kv_capture": [P, P, I, P, P, P],
         "qi_dit_check": [P, P],
         "qi_dit_block_forward": [P, I, P, I, I, F, P, P, P],
@@ -366,6 +367,54 @@ class DiT:
         _check(lib().qi_dit_step(self._h, hp(img_tokens), N, hp(txt_feats), L, float(timestep), hp(txt_cos),
                                  hp(txt_sin), hp(img_cos), hp(img_sin), hp(vel), flags, _stream(stream)))
         return vel
+
+    def euler_step(self, x, txt_feats, L: int, timestep: float, sigma_i: float, sigma_next: float, txt_cos, txt_sin,
+                   img_cos, img_sin, use_cache: bool = False, vel=None, stream=None):
+        """One sampler step on device tensors: the DiT pass on x [N, 64], then x += (sigma_next - sigma_i) * vel
+        in place. txt_* may be None with use_cache. vel (optional, [N, 64]) receives the velocity."""
+        N = x.shape[0]
+        _dev_f32(x, (N, PATCH), "x")
+        _dev_f32(img_cos, (N, ROPE_COLS), "img_cos")
+        _dev_f32(img_sin, (N, ROPE_COLS), "img_sin")
+        if not use_cache:
+            _dev_f32(txt_feats, (L, HIDDEN), "txt_feats")
+            _dev_f32(txt_cos, (L, ROPE_COLS), "txt_cos")
+            _dev_f32(txt_sin, (L, ROPE_COLS), "txt_sin")
+        if vel is not None:
+            _dev_f32(vel, (N, PATCH), "vel")
+        flags = STEP_USE_CACHE if use_cache else STEP_JOINT
+        _check(lib().qi_dit_euler_step(self._h, _ptr(x), N, None if use_cache else _ptr(txt_feats), L,
+                                       float(timestep), float(sigma_i), float(sigma_next),
+                                       None if use_cache else _ptr(txt_cos), None if use_cache else _ptr(txt_sin),
+                                       _ptr(img_cos), _ptr(img_sin), _ptr(vel), flags, _stream(stream)))
+        return x
+
+    def euler_step_host(self, x, txt_feats, L: int, timestep: float, sigma_i: float, sigma_next: float, txt_cos,
+                        txt_sin, img_cos, img_sin, use_cache: bool = False, vel=None, stream=None):
+        """The same sampler step on HOST buffers (numpy arrays or pinned torch CPU tensors, float32,
+        contiguous): the call copies in, runs, copies x (and vel) back and synchronises."""
+        def hp(a, name, shape):
+            if a is None:
+                return None
+            if isinstance(a, np.ndarray):
+                ok = a.dtype == np.float32 and a.flags["C_CONTIGUOUS"] and a.shape == shape
+                ptr = a.ctypes.data
+            else:
+                import torch
+                ok = a.dtype == torch.float32 and not a.is_cuda and a.is_contiguous() and tuple(a.shape) == shape
+                ptr = a.data_ptr()
+            if not ok:
+                raise ValueError(f"{name}: want a contiguous float32 host array {shape}")
+            return ptr
+        N = x.shape[0]
+        flags = STEP_HOST_IO | (STEP_USE_CACHE if use_cache else 0)
+        t = (lambda a, n, sh: None) if use_cache else hp
+        _check(lib().qi_dit_euler_step(self._h, hp(x, "x", (N, PATCH)), N, t(txt_feats, "txt_feats", (L, HIDDEN)), L,
+                                       float(timestep), float(sigma_i), float(sigma_next),
+                                       t(txt_cos, "txt_cos", (L, ROPE_COLS)), t(txt_sin, "txt_sin", (L, ROPE_COLS)),
+                                       hp(img_cos, "img_cos", (N, ROPE_COLS)), hp(img_sin, "img_sin", (N, ROPE_COLS)),
+                                       hp(vel, "vel", (N, PATCH)), flags, _stream(stream)))
+        return x
 
     def step_cfg(self, img_tokens, timestep: float, guidance: float, pos, neg, use_cache: bool = False, vel=None,
                  stream=None):

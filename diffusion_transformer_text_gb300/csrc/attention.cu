@@ -345,12 +345,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
   if (p.Rq <= 0) return cudaSuccess;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = ensure_smem_limit(attn_tc, kSmem, attr_done);
+  if (e != cudaSuccess) return e;
   CUtensorMap mq, mk, mv;
   if (!encode_map16(&mq, p.q, p.Rq, kHidden, kBQ, false) || !encode_map16(&mk, p.k, p.Lk, kHidden, kBKV, false) ||
       !encode_map16(&mv, p.v, p.Lk, kHidden, kBKV, false))

@@ -822,12 +822,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 template <int KIND>
 cudaError_t launch_pair_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
                              cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_pair_tc<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = ensure_smem_limit(gemm_pair_tc<KIND>, kPairSmem, attr_done);
+  if (e != cudaSuccess) return e;
   return launch_dependent(gemm_pair_tc<KIND>, dim3(grid), dim3(192), kPairSmem, stream, a, b, p);
 }
 
@@ -861,12 +858,9 @@ cudaError_t launch_pair_any(EpiKind kind, const CUtensorMap& a, const CUtensorMa
 template <int KIND>
 cudaError_t launch_mx_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
                            cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_mx_tc<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, MxGeo::kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = ensure_smem_limit(gemm_mx_tc<KIND>, MxGeo::kSmem, attr_done);
+  if (e != cudaSuccess) return e;
   return launch_dependent(gemm_mx_tc<KIND>, dim3(grid), dim3(192), MxGeo::kSmem, stream, a, b, p);
 }
 

@@ -10,9 +10,12 @@
 //
 // The first call on a device does the set-up (the array's device address is
 // looked up once, with that device current); make it before any stream
-// capture. All calls on a device share the array and the last call's status
-// stays in it: each call clears the word first, so calls that overlap on the
-// GPU race on it and must be serialised by the caller.
+// capture. The address is kept for the life of the process, so the entry point
+// must not be used on a device after cudaDeviceReset (or any other teardown of
+// the device's primary context) in the same process. All calls on a device
+// share the array and the last call's status stays in it: each call clears the
+// word first, so calls that overlap on the GPU race on it and must be
+// serialised by the caller.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -30,9 +33,10 @@ namespace {
 constexpr int kStatusWords = 64;
 static __device__ __align__(256) int g_noalloc_status[kStatusWords];
 
-// Largest shapes accepted: those of the DiT's own GEMMs (rows of the longest
-// pass, the stacked gate/up width, the SwiGLU inner width).
-constexpr int kMaxM = QI_L_MAX + QI_N_MAX;
+// Largest shapes accepted: those of the DiT's own GEMMs. Rows: the longer of a
+// joint pass (L + N) and the batch-2 image-only guidance pass (2 N); columns: the
+// stacked gate/up width; contraction: the SwiGLU inner width.
+constexpr int kMaxM = QI_L_MAX + QI_N_MAX > 2 * QI_N_MAX ? QI_L_MAX + QI_N_MAX : 2 * QI_N_MAX;
 constexpr int kMaxN = 2 * QI_FFN;
 constexpr int kMaxK = QI_FFN;
 constexpr int kMaxDevices = 64;
@@ -44,36 +48,12 @@ struct DeviceSlot {
 DeviceSlot g_slots[kMaxDevices];
 std::mutex g_slots_mu;
 
-qi_status noalloc_fail(qi_status st, const char* msg, int a = 0, int b = 0, int c = 0) {
+qi_status noalloc_fail(qi_status st, const char* fmt, int a = 0, int b = 0, int c = 0, int d = 0, int e = 0,
+                       int f = 0) {
   char buf[256];
-  snprintf(buf, sizeof(buf), msg, a, b, c);
+  snprintf(buf, sizeof(buf), fmt, a, b, c, d, e, f);
   qi::set_last_error(buf);  // read back with qi_last_error()
   return st;
-}
-
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-bool encode_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  static EncodeFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeFn>(p);
-  });
-  if (!fn) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Once per device, with that device current: look up the array's device address.
@@ -109,8 +89,8 @@ extern "C" qi_status qi_gemm_bf16_noalloc(const uint16_t* A, const uint16_t* B, 
     return noalloc_fail(QI_ERR_SHAPE, "qi_gemm_bf16_noalloc: M %d N %d K %d (need N %% 256 == 0, K %% 64 == 0)", M,
                         N, K);
   if (M > kMaxM || N > kMaxN || K > kMaxK)
-    return noalloc_fail(QI_ERR_SHAPE, "qi_gemm_bf16_noalloc: M %d N %d K %d above the limits 16896 x 24576 x 12288",
-                        M, N, K);
+    return noalloc_fail(QI_ERR_SHAPE, "qi_gemm_bf16_noalloc: M %d N %d K %d above the limits %d x %d x %d", M, N, K,
+                        kMaxM, kMaxN, kMaxK);
   if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15) ||
       (reinterpret_cast<uintptr_t>(D) & 15))
     return noalloc_fail(QI_ERR_INVALID_ARG, "qi_gemm_bf16_noalloc: A, B and D must be 16-byte aligned");
@@ -118,7 +98,8 @@ extern "C" qi_status qi_gemm_bf16_noalloc(const uint16_t* A, const uint16_t* B, 
   qi_status st = device_slot(&slot);
   if (st != QI_OK) return st;
   CUtensorMap ma, mb;
-  if (!encode_map(&ma, A, M, K, 128) || !encode_map(&mb, B, N, K, qi::kBoxRowsPair))
+  // the same bf16 maps qi_gemm_bf16 builds, so both entry points run identical launches
+  if (!qi::encode_map16(&ma, A, M, K, 128, true) || !qi::encode_map16(&mb, B, N, K, qi::kBoxRowsPair, true))
     return noalloc_fail(QI_ERR_CUDA, "qi_gemm_bf16_noalloc: tensor map encoding failed");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the status word must start at zero for this call

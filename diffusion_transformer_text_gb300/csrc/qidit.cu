@@ -572,6 +572,54 @@ bool all_loaded(const qi_dit* d) {
   return true;
 }
 
+// Argument checks shared by the single-prompt step entry points. `vel` is the
+// velocity output, or for the sampler step any non-NULL pointer.
+qi_status step_checks(qi_dit* d, const char* who, const void* img, int N, const float* txt, int L, float t,
+                      const float* tc, const float* ts, const float* ic, const float* is, const void* vel,
+                      unsigned flags) {
+  if (!d) return fail(QI_ERR_INVALID_ARG, "%s: NULL handle", who);
+  if (flags & ~(QI_STEP_USE_CACHE | QI_STEP_HOST_IO)) return fail(QI_ERR_INVALID_ARG, "%s: flags %u", who, flags);
+  const bool use_cache = flags & QI_STEP_USE_CACHE;
+  if (N < QI_N_MIN || N > d->N_max || L < QI_L_MIN || L > d->L_max)
+    return fail(QI_ERR_SHAPE, "%s: N %d (max %d) L %d (max %d)", who, N, d->N_max, L, d->L_max);
+  if (!img || !ic || !is || !vel) return fail(QI_ERR_INVALID_ARG, "%s: NULL image tensor", who);
+  if (!use_cache && (!txt || !tc || !ts))
+    return fail(QI_ERR_INVALID_ARG, "%s: joint pass needs txt_feats and txt_cos/txt_sin", who);
+  if (use_cache && d->cache_L[0] != L)
+    return fail(QI_ERR_STATE, "%s: USE_CACHE but the text K/V capture is for L=%d, not %d", who, d->cache_L[0], L);
+  if (!all_loaded(d)) return fail(QI_ERR_STATE, "%s: weights not loaded", who);
+  if (!std::isfinite(t)) return fail(QI_ERR_INVALID_ARG, "%s: timestep not finite", who);
+  return QI_OK;
+}
+
+// Device staging for host-buffer steps (allocated on first use, held until destroy).
+qi_status ensure_staging(qi_dit* d) {
+  // each buffer once: a failed call leaves the ones it made for the next call
+  if (!d->st_vel) QI_ALLOC(d->st_vel, (size_t)d->N_max * kPatch * 4);
+  if (!d->st_ic) QI_ALLOC(d->st_ic, (size_t)d->N_max * kRopeCols * 4);
+  if (!d->st_is) QI_ALLOC(d->st_is, (size_t)d->N_max * kRopeCols * 4);
+  if (!d->st_txt) QI_ALLOC(d->st_txt, (size_t)d->L_max * kHidden * 4);
+  if (!d->st_tc) QI_ALLOC(d->st_tc, (size_t)d->L_max * kRopeCols * 4);
+  if (!d->st_ts) QI_ALLOC(d->st_ts, (size_t)d->L_max * kRopeCols * 4);
+  if (!d->st_img) QI_ALLOC(d->st_img, (size_t)d->N_max * kPatch * 4);
+  return QI_OK;
+}
+
+// Host -> staging copies of a step's inputs (the text ones only for a joint pass).
+qi_status stage_inputs(qi_dit* d, const float* img, int N, const float* txt, int L, const float* tc, const float* ts,
+                       const float* ic, const float* is, bool use_cache, cudaStream_t s) {
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
+  QI_CUDA(cudaMemcpyAsync(d->st_img, img, (size_t)N * kPatch * 4, h2d, s));
+  QI_CUDA(cudaMemcpyAsync(d->st_ic, ic, (size_t)N * kRopeCols * 4, h2d, s));
+  QI_CUDA(cudaMemcpyAsync(d->st_is, is, (size_t)N * kRopeCols * 4, h2d, s));
+  if (!use_cache) {
+    QI_CUDA(cudaMemcpyAsync(d->st_txt, txt, (size_t)L * kHidden * 4, h2d, s));
+    QI_CUDA(cudaMemcpyAsync(d->st_tc, tc, (size_t)L * kRopeCols * 4, h2d, s));
+    QI_CUDA(cudaMemcpyAsync(d->st_ts, ts, (size_t)L * kRopeCols * 4, h2d, s));
+  }
+  return QI_OK;
+}
+
 }  // namespace
 
 void qi::set_last_error(const char* msg) { g_last_error = msg; }
@@ -983,41 +1031,15 @@ qi_status qi_dpmpp2m_update(float* x, const float* vel, float* d_prev, int N, co
 qi_status qi_dit_step(qi_dit* d, const float* img_tokens, int N, const float* txt_feats, int L, float timestep,
                       const float* txt_cos, const float* txt_sin, const float* img_cos, const float* img_sin,
                       float* vel, unsigned flags, qi_stream_t stream) {
-  if (!d) return fail(QI_ERR_INVALID_ARG, "qi_dit_step: NULL handle");
-  if (flags & ~(QI_STEP_USE_CACHE | QI_STEP_HOST_IO)) return fail(QI_ERR_INVALID_ARG, "qi_dit_step: flags %u", flags);
+  QI_TRY(step_checks(d, "qi_dit_step", img_tokens, N, txt_feats, L, timestep, txt_cos, txt_sin, img_cos, img_sin, vel,
+                     flags));
   const bool use_cache = flags & QI_STEP_USE_CACHE;
-  const bool host_io = flags & QI_STEP_HOST_IO;
-  if (N < QI_N_MIN || N > d->N_max || L < QI_L_MIN || L > d->L_max)
-    return fail(QI_ERR_SHAPE, "qi_dit_step: N %d (max %d) L %d (max %d)", N, d->N_max, L, d->L_max);
-  if (!img_tokens || !img_cos || !img_sin || !vel) return fail(QI_ERR_INVALID_ARG, "qi_dit_step: NULL image tensor");
-  if (!use_cache && (!txt_feats || !txt_cos || !txt_sin))
-    return fail(QI_ERR_INVALID_ARG, "qi_dit_step: joint pass needs txt_feats and txt_cos/txt_sin");
-  if (use_cache && d->cache_L[0] != L)
-    return fail(QI_ERR_STATE, "qi_dit_step: USE_CACHE but the text K/V capture is for L=%d, not %d", d->cache_L[0], L);
-  if (!all_loaded(d)) return fail(QI_ERR_STATE, "qi_dit_step: weights not loaded");
-  if (!std::isfinite(timestep)) return fail(QI_ERR_INVALID_ARG, "qi_dit_step: timestep not finite");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   QI_CUDA(cudaSetDevice(d->device));
 
-  if (host_io) {
-    if (!d->st_img) {
-      QI_ALLOC(d->st_img, (size_t)d->N_max * kPatch * 4);
-      QI_ALLOC(d->st_vel, (size_t)d->N_max * kPatch * 4);
-      QI_ALLOC(d->st_ic, (size_t)d->N_max * kRopeCols * 4);
-      QI_ALLOC(d->st_is, (size_t)d->N_max * kRopeCols * 4);
-      QI_ALLOC(d->st_txt, (size_t)d->L_max * kHidden * 4);
-      QI_ALLOC(d->st_tc, (size_t)d->L_max * kRopeCols * 4);
-      QI_ALLOC(d->st_ts, (size_t)d->L_max * kRopeCols * 4);
-    }
-    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
-    QI_CUDA(cudaMemcpyAsync(d->st_img, img_tokens, (size_t)N * kPatch * 4, h2d, s));
-    QI_CUDA(cudaMemcpyAsync(d->st_ic, img_cos, (size_t)N * kRopeCols * 4, h2d, s));
-    QI_CUDA(cudaMemcpyAsync(d->st_is, img_sin, (size_t)N * kRopeCols * 4, h2d, s));
-    if (!use_cache) {
-      QI_CUDA(cudaMemcpyAsync(d->st_txt, txt_feats, (size_t)L * kHidden * 4, h2d, s));
-      QI_CUDA(cudaMemcpyAsync(d->st_tc, txt_cos, (size_t)L * kRopeCols * 4, h2d, s));
-      QI_CUDA(cudaMemcpyAsync(d->st_ts, txt_sin, (size_t)L * kRopeCols * 4, h2d, s));
-    }
+  if (flags & QI_STEP_HOST_IO) {
+    QI_TRY(ensure_staging(d));
+    QI_TRY(stage_inputs(d, img_tokens, N, txt_feats, L, txt_cos, txt_sin, img_cos, img_sin, use_cache, s));
     QI_TRY(run_pass(d, 0, use_cache ? kImage : kJoint, d->st_img, N, d->st_txt, L, timestep, d->st_tc, d->st_ts,
                     d->st_ic, d->st_is, d->st_vel, s));
     QI_CUDA(cudaMemcpyAsync(vel, d->st_vel, (size_t)N * kPatch * 4, cudaMemcpyDeviceToHost, s));
@@ -1026,6 +1048,42 @@ qi_status qi_dit_step(qi_dit* d, const float* img_tokens, int N, const float* tx
   }
   QI_TRY(run_pass(d, 0, use_cache ? kImage : kJoint, img_tokens, N, txt_feats, L, timestep, txt_cos, txt_sin,
                   img_cos, img_sin, vel, s));
+  if (!use_cache) d->cache_L[0] = L;
+  return QI_OK;
+}
+
+qi_status qi_dit_euler_step(qi_dit* d, float* x, int N, const float* txt_feats, int L, float timestep, float sigma_i,
+                            float sigma_next, const float* txt_cos, const float* txt_sin, const float* img_cos,
+                            const float* img_sin, float* vel_out, unsigned flags, qi_stream_t stream) {
+  // vel_out may be NULL: the step then keeps the velocity in the handle's staging buffer
+  QI_TRY(step_checks(d, "qi_dit_euler_step", x, N, txt_feats, L, timestep, txt_cos, txt_sin, img_cos, img_sin, x,
+                     flags));
+  if (!std::isfinite(sigma_i) || !std::isfinite(sigma_next))
+    return fail(QI_ERR_INVALID_ARG, "qi_dit_euler_step: sigmas not finite");
+  const bool use_cache = flags & QI_STEP_USE_CACHE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  QI_CUDA(cudaSetDevice(d->device));
+  const long long n = static_cast<long long>(N) * kPatch;
+
+  if (flags & QI_STEP_HOST_IO) {
+    QI_TRY(ensure_staging(d));
+    QI_TRY(stage_inputs(d, x, N, txt_feats, L, txt_cos, txt_sin, img_cos, img_sin, use_cache, s));
+    QI_TRY(run_pass(d, 0, use_cache ? kImage : kJoint, d->st_img, N, d->st_txt, L, timestep, d->st_tc, d->st_ts,
+                    d->st_ic, d->st_is, d->st_vel, s));
+    QI_CUDA(qi::launch_euler(d->st_img, d->st_vel, n, sigma_i, sigma_next, s));
+    QI_CUDA(cudaMemcpyAsync(x, d->st_img, static_cast<size_t>(n) * 4, cudaMemcpyDeviceToHost, s));
+    if (vel_out) QI_CUDA(cudaMemcpyAsync(vel_out, d->st_vel, static_cast<size_t>(n) * 4, cudaMemcpyDeviceToHost, s));
+    if (!use_cache) d->cache_L[0] = L;
+    return check_device_word(d, s);
+  }
+  float* vel = vel_out;
+  if (!vel) {
+    QI_TRY(ensure_staging(d));
+    vel = d->st_vel;
+  }
+  QI_TRY(run_pass(d, 0, use_cache ? kImage : kJoint, x, N, txt_feats, L, timestep, txt_cos, txt_sin, img_cos, img_sin,
+                  vel, s));
+  QI_CUDA(qi::launch_euler(x, vel, n, sigma_i, sigma_next, s));
   if (!use_cache) d->cache_L[0] = L;
   return QI_OK;
 }

@@ -246,6 +246,26 @@ qi_status qi_dit_step(qi_dit* dit, const float* img_tokens, int N, const float* 
                       const float* img_cos, const float* img_sin, float* vel, unsigned flags,
                       qi_stream_t stream);
 
+/* One FlowMatch Euler sampler step [HOST s6; ARCH]: the DiT pass of qi_dit_step
+ * with x (the latent tokens [N, 64], float32) as img_tokens, then the Euler update
+ * of qi_euler_update in place, x <- x + (sigma_next - sigma_i) * vel (each
+ * operation rounded on its own), so one call advances the sampler by one step.
+ * Arguments and flags as qi_dit_step; timestep is the DiT input of the step
+ * (timesteps[i] / 1000), sigma_i and sigma_next its two sigmas. vel_out [N, 64]
+ * receives the velocity; it may be NULL, and then the velocity stays in the
+ * handle's staging buffer. With QI_STEP_HOST_IO, x (in and out), txt_feats, the
+ * four tables and vel_out are HOST pointers (pinned memory copies fastest): the
+ * call copies the inputs in, x (and vel_out) out, and synchronises `stream`
+ * before returning, reporting a device-word error as qi_dit_check does.
+ * The first call with host buffers or a NULL vel_out allocates the staging
+ * buffers (inputs and velocity for N_max and L_max rows, held until destroy).
+ * x, vel_out: element-wise identical to qi_dit_step followed by qi_euler_update.
+ * Errors: as qi_dit_step; INVALID_ARG for non-finite sigmas; OOM for staging. */
+qi_status qi_dit_euler_step(qi_dit* dit, float* x, int N, const float* txt_feats, int L, float timestep,
+                            float sigma_i, float sigma_next, const float* txt_cos, const float* txt_sin,
+                            const float* img_cos, const float* img_sin, float* vel_out, unsigned flags,
+                            qi_stream_t stream);
+
 /* Classifier-free guidance step [MLX page, "Optional modes": the negative
  * prompt is used as noise = neg + g * (pos - neg), with its K/V in a second
  * slot ("Text K/V reuse")]. Runs the pass of qi_dit_step for the conditional
@@ -395,12 +415,15 @@ qi_status qi_gemm_mxfp8(qi_dit* dit, const uint8_t* A, const uint8_t* A_sf, cons
  * Scratch: the kernel's status word sits in a 256-byte static device array
  * that the library holds on every device that loads it, until exit. The first
  * call on a device (the device current at the call) looks the array up with
- * cudaGetSymbolAddress; make that first call before any stream capture. Every
- * call clears the status word, then the kernel reports into it, so calls that
- * overlap on the GPU (other streams, other threads) race on it; serialise them.
- * Limits: N % 256 == 0, K % 64 == 0, M <= 16896, N <= 24576, K <= 12288 (the
- * DiT's own GEMM shapes); larger sizes return QI_ERR_SHAPE with a message in
- * qi_last_error(). sync_check != 0 synchronises `stream` and returns
+ * cudaGetSymbolAddress; make that first call before any stream capture. The
+ * address is kept for the life of the process: do not use this entry point on
+ * a device after cudaDeviceReset (or another teardown of its primary context).
+ * Every call clears the status word, then the kernel reports into it, so calls
+ * that overlap on the GPU (other streams, other threads) race on it; serialise
+ * them. Limits: N % 256 == 0, K % 64 == 0, M <= 32768, N <= 24576, K <= 12288
+ * (the DiT's own GEMM shapes: rows of a joint pass, L + N <= 16896, or of the
+ * batch-2 guidance pass, 2 N <= 32768); larger sizes return QI_ERR_SHAPE with a
+ * message in qi_last_error(). sync_check != 0 synchronises `stream` and returns
  * QI_ERR_DEVICE_TIMEOUT if a bounded wait in the kernel expired. */
 qi_status qi_gemm_bf16_noalloc(const uint16_t* A, const uint16_t* B, float* D, int M, int N, int K,
                                int sync_check, qi_stream_t stream);

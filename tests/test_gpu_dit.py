@@ -129,6 +129,49 @@ def test_reuse_equals_joint_bit_exact(qi, dit256):
     assert np.array_equal(c2.cpu().numpy(), j2.cpu().numpy())
 
 
+def test_euler_step_equals_step_then_update(qi, dit256):
+    """qi_dit_euler_step (device and host buffers) = qi_dit_step then qi_euler_update, bit for bit,
+    for a joint step and a cached step; the host call returns x and vel in the caller's buffers."""
+    import torch
+    case, W, d = dit256
+    sig, ts_ = qi.flow_sigmas(40, case.N)
+    img0 = synth.img_tokens(case)
+    txt = synth.txt_feats(case)
+    tabs = _tables(case.L, case.h, case.w)
+    tc, ts, ic, is_ = [f32_tensor(a) for a in tabs]
+    txt_d = f32_tensor(txt)
+    for i, use_cache in ((0, False), (1, True)):
+        t = float(np.float32(ts_[i]) / np.float32(1000.0))
+        # reference: the two calls
+        x_ref = f32_tensor(img0)
+        v_ref = d.step(x_ref, None if use_cache else txt_d, t, None if use_cache else tc, None if use_cache else ts,
+                       ic, is_, use_cache=use_cache).clone()
+        qi.euler_update(x_ref, v_ref, float(sig[i]), float(sig[i + 1]))
+        # device sampler step
+        x_dev = f32_tensor(img0)
+        v_dev = torch.empty_like(x_dev)
+        d.euler_step(x_dev, None if use_cache else txt_d, case.L, t, float(sig[i]), float(sig[i + 1]),
+                     None if use_cache else tc, None if use_cache else ts, ic, is_, use_cache=use_cache, vel=v_dev)
+        # host sampler step (pinned buffers), and with vel_out NULL
+        x_h = torch.from_numpy(img0.copy()).pin_memory()
+        v_h = torch.empty(case.N, 64).pin_memory()
+        host = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in tabs]
+        txt_h = torch.from_numpy(txt.copy()).pin_memory()
+        d.euler_step_host(x_h, txt_h, case.L, t, float(sig[i]), float(sig[i + 1]), host[0], host[1], host[2], host[3],
+                          use_cache=use_cache, vel=v_h)
+        x_n = img0.copy()
+        d.euler_step_host(x_n, None if use_cache else txt, case.L, t, float(sig[i]), float(sig[i + 1]),
+                          None if use_cache else np.ascontiguousarray(tabs[0]),
+                          None if use_cache else np.ascontiguousarray(tabs[1]), np.ascontiguousarray(tabs[2]),
+                          np.ascontiguousarray(tabs[3]), use_cache=use_cache)
+        d.check()
+        xr, vr = x_ref.cpu().numpy(), v_ref.cpu().numpy()
+        assert np.array_equal(x_dev.cpu().numpy(), xr) and np.array_equal(v_dev.cpu().numpy(), vr)
+        assert np.array_equal(x_h.numpy(), xr) and np.array_equal(v_h.numpy(), vr)
+        assert np.array_equal(x_n, xr)
+        assert not np.array_equal(xr, img0)
+
+
 def test_text_only_capture_equals_joint(qi, dit256):
     """A text-only pass stores the same text K/V as a joint pass, bit for bit."""
     case, W, d = dit256

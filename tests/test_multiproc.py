@@ -79,3 +79,30 @@ def test_step_mix():
     assert bench.step_mix(1) == (1, 0)
     cfg = bench.arm_config(4, 80)
     assert cfg["joint_steps"] == 2 and cfg["image_only_steps"] == 78 and cfg["global_batch"] == 4
+
+
+def test_bench_flop_model_matches_the_oracle_accounting():
+    """The bench's per-pass and per-kernel-class FLOPs equal the oracle's step model on every workload."""
+    import bench
+    from oracle import dit as odit
+    for case in (synth_cases()):
+        for joint in (True, False):
+            R = case.L + case.N if joint else case.N
+            want = odit.step_flops(R, case.N, case.L, joint)
+            assert bench.pass_flops(case.L, case.N, joint) == want
+            assert sum(bench.class_flops(case.L, case.N, joint).values()) == want
+    # 598 rows at 384^2 with a 22-token prompt: about 8.5 TFLOP (MLX page, "Where the time goes")
+    assert abs(bench.pass_flops(22, 576, True) / 1e12 - 8.5) < 0.05
+
+
+def test_bench_clock_normalised_fraction():
+    import bench
+    # the same TFLOP/s per MHz as the peak is a fraction of 1, whatever the two clocks
+    assert abs(bench.frac_at_clock(1000.0, 1500.0, 1200.0, 1800.0) - 1.0) < 1e-12
+    assert abs(bench.frac_at_clock(1715.5, 1650.0, 1741.2, 1492.0) - 0.8909) < 1e-3
+    assert bench.frac_at_clock(1000.0, None, 1200.0, 1800.0) is None
+
+
+def synth_cases():
+    import synth
+    return (synth.STEP_256, synth.STEP_384_L22, synth.STEP_384_L494, synth.LOOP_1024, synth.STEP_2048)
