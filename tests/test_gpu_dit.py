@@ -144,8 +144,10 @@ def test_euler_step_equals_step_then_update(qi, dit256):
         t = float(np.float32(ts_[i]) / np.float32(1000.0))
         # reference: the two calls
         x_ref = f32_tensor(img0)
-        v_ref = d.step(x_ref, None if use_cache else txt_d, t, None if use_cache else tc, None if use_cache else ts,
-                       ic, is_, use_cache=use_cache).clone()
+        if use_cache:
+            v_ref = d.step_cached(x_ref, case.L, t, ic, is_).clone()
+        else:
+            v_ref = d.step(x_ref, txt_d, t, tc, ts, ic, is_).clone()
         qi.euler_update(x_ref, v_ref, float(sig[i]), float(sig[i + 1]))
         # device sampler step
         x_dev = f32_tensor(img0)
