@@ -26,6 +26,7 @@ STEP_JOINT = 0
 STEP_USE_CACHE = 1
 STEP_HOST_IO = 2
 PROF_CLASSES = ("qkv_gemm", "attention", "out_gemm", "gateup_gemm", "down_gemm", "other")
+RANGE_KINDS = ("x_mod1", "q_rope", "k_rope", "v", "o", "x_mod2", "h", "txt_in")
 
 STATUS = {
     0: "QI_OK", 1: "QI_ERR_INVALID_ARG", 2: "QI_ERR_SHAPE", 3: "QI_ERR_STATE", 4: "QI_ERR_OOM",
@@ -40,7 +41,7 @@ SYMBOLS = (
     "qi_dit_block_forward", "qi_dit_read_kv", "qi_dit_set_trace", "qi_dit_profile", "qi_dit_profile_classes",
     "qi_dit_profile_read", "qi_last_error", "qi_gemm_bf16", "qi_attention_f16", "qi_gemm_bf16_noalloc",
     "qi_dit_step_cfg", "qi_dpmpp2m_coeffs", "qi_dpmpp2m_update", "qi_dit_step_fbcache", "qi_dit_fbcache_reset",
-    "qi_dit_set_mxfp8", "qi_quant_mxfp8", "qi_gemm_mxfp8", "qi_debug_inject", "qi_dit_euler_step",
+    "qi_dit_set_mxfp8", "qi_quant_mxfp8", "qi_gemm_mxfp8", "qi_debug_inject", "qi_dit_euler_step", "qi_dit_set_range_probe",
 )
 
 
@@ -103,6 +104,7 @@ def lib() -> ctypes.CDLL:
         "qi_dit_block_forward": [P, I, P, I, I, F, P, P, P],
         "qi_dit_read_kv": [P, I, I, I, P, P, P],
         "qi_dit_set_trace": [P, I, I, P],
+        "qi_dit_set_range_probe": [P, P],
         "qi_dit_profile": [P, I],
         "qi_dit_profile_classes": [P, U, I],
         "qi_dit_profile_read": [P, P, P],
@@ -504,6 +506,13 @@ class DiT:
     def set_mxfp8(self, on: bool):
         """Run later passes on MXFP8 block GEMMs (handle created with mxfp8=True)."""
         _check(lib().qi_dit_set_mxfp8(self._h, int(on)))
+
+    def set_range_probe(self, out=None):
+        """Test hook: while `out` (float32 cuda [blocks, 8], zeroed) is set, passes fold the largest
+        |value| of each fp16 operand per block into it (kinds in RANGE_KINDS); None turns it off."""
+        if out is not None:
+            _dev_f32(out, (self.blocks, len(RANGE_KINDS)), "out")
+        _check(lib().qi_dit_set_range_probe(self._h, _ptr(out)))
 
     def set_trace(self, slot: int, block: int, dst=None):
         _check(lib().qi_dit_set_trace(self._h, slot, block, _ptr(dst)))

@@ -222,6 +222,10 @@ cudaError_t launch_cfg_combine(const float* pos, const float* neg, float g, floa
 // magnitude exceeds the fp16 range are counted into *overflow.
 cudaError_t launch_bf16_to_f16(uint16_t* w, size_t n, unsigned int* overflow, cudaStream_t s);
 
+// Test hook (operand ranges): *out = max(*out, max |a[i]|) over n fp16 values
+// (n a multiple of 8, a 16-byte aligned); NaN counts as +inf.
+cudaError_t launch_absmax_f16(const act_t* a, long long n, float* out, cudaStream_t s);
+
 // Sets the calling thread's message returned by qi_last_error() (qidit.cu).
 void set_last_error(const char* msg);
 

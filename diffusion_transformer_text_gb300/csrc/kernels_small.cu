@@ -604,6 +604,29 @@ __global__ void bf16_to_f16_kernel(uint32_t* w, size_t pairs, unsigned int* over
   if (bad) atomicAdd(overflow, bad);
 }
 
+// Largest magnitude of an fp16 tensor (n a multiple of 8, 16-byte aligned) into
+// *out with an atomic max on the float's bits (non-negative floats order like
+// their bit patterns); a NaN counts as +inf, so an overflow cannot hide.
+__global__ void absmax_f16_kernel(const uint4* a, long long n8, float* out) {
+  float m = 0.f;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const uint4 w = a[i];
+    const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2 hv = *reinterpret_cast<const __half2*>(&v[k]);
+      const float2 f = __half22float2(hv);
+      const float a0 = fabsf(f.x), a1 = fabsf(f.y);
+      m = fmaxf(m, a0 != a0 ? INFINITY : a0);
+      m = fmaxf(m, a1 != a1 ? INFINITY : a1);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<int*>(out), __float_as_int(m));
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- launchers
@@ -665,6 +688,15 @@ cudaError_t launch_bf16_to_f16(uint16_t* w, size_t n, unsigned int* overflow, cu
   const size_t want = (pairs + 255) / 256;
   const unsigned blocks = static_cast<unsigned>(want < 148 * 32 ? want : 148 * 32);
   bf16_to_f16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<uint32_t*>(w), pairs, overflow);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_absmax_f16(const act_t* a, long long n, float* out, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const long long n8 = n / 8;
+  const long long want = (n8 + 255) / 256;
+  absmax_f16_kernel<<<static_cast<unsigned>(want < 1216 ? want : 1216), 256, 0, s>>>(reinterpret_cast<const uint4*>(a),
+                                                                                      n8, out);
   return cudaGetLastError();
 }
 

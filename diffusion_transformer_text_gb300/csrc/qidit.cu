@@ -202,6 +202,7 @@ struct qi_dit {
 
   int trace_block[2] = {-1, -1};
   float* trace_dst[2] = {nullptr, nullptr};
+  float* range_out = nullptr;  // test hook: [blocks][QI_RANGE_KINDS] max |fp16 operand| (qi_dit_set_range_probe)
 
   unsigned prof_mask = 0;  // kernel classes timed with events (bit c = class c)
   int prof_stride = 1;     // block-level classes: only blocks b % prof_stride == 0
@@ -255,6 +256,13 @@ qi_status check_device_word(qi_dit* d, cudaStream_t s) {
     if (h == qi::kErrNonFinite) return fail(QI_ERR_NONFINITE, "the DiT pass produced a non-finite velocity");
     return fail(QI_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired (device code %d)", h);
   }
+  return QI_OK;
+}
+
+// Operand-range test hook: fold max |a| over n fp16 values into the block's `kind` slot.
+qi_status probe(qi_dit* d, int block, int kind, const act_t* a, long long n, cudaStream_t s) {
+  if (!d->range_out || d->mx_on) return QI_OK;
+  QI_CUDA(qi::launch_absmax_f16(a, n, d->range_out + block * QI_RANGE_KINDS + kind, s));
   return QI_OK;
 }
 
@@ -318,6 +326,10 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
   p.err = d->err;
   p.stall_test = d->inject_stall;  // one-shot: only this block's QKV GEMM carries it
   d->inject_stall = 0;
+  // operand ranges (test hook) of single-prompt passes
+  const bool rp = d->range_out && two.split == 0;
+  const long long RH = static_cast<long long>(R) * kHidden;
+  if (rp) QI_TRY(probe(d, b, 0, d->xa, RH, s));
 
   // QKV + 1/rms + RoPE -> Q and this block's K/V store
   {
@@ -347,6 +359,11 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
     QI_TRY(block_gemm(d, qi::kEpiQkv, d->xa, R, kHidden, m_xa, B.m_qkv, BM ? BM->m_qkv : B.m_qkv,
                       BM ? BM->sqkv : nullptr, g, s));
     p.stall_test = 0;
+  }
+  if (rp) {
+    QI_TRY(probe(d, b, 1, d->q, RH, s));
+    QI_TRY(probe(d, b, 2, d->k_of(b) + static_cast<size_t>(q_off) * kHidden, RH, s));
+    QI_TRY(probe(d, b, 3, d->v_of(b) + static_cast<size_t>(q_off) * kHidden, RH, s));
   }
   // block-causal attention
   {
@@ -384,6 +401,7 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
       QI_CUDA(qi::launch_attention(a, s));
     }
   }
+  if (rp) QI_TRY(probe(d, b, 4, d->o, RH, s));
   // out-projection: x += g1 * (o Wo^T); xa = fp16(x (1 + s2))
   {
     ProfScope ps(d, s, 2, b);
@@ -399,6 +417,7 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
     QI_TRY(block_gemm(d, qi::kEpiResid, d->o, R, kHidden, m_o, B.m_o, BM ? BM->m_o : B.m_o, BM ? BM->so : nullptr, g,
                       s, BM ? d->aq : nullptr, BM ? d->asf : nullptr));
   }
+  if (rp) QI_TRY(probe(d, b, 5, d->xa, RH, s));
   // gate/up + SwiGLU
   {
     ProfScope ps(d, s, 3, b);
@@ -415,6 +434,7 @@ qi_status run_block(qi_dit* d, int b, int R, int n_text, int q_off, int L, int L
     QI_TRY(block_gemm(d, qi::kEpiSwiglu, d->xa, R, kHidden, m_xa, B.m_gu, BM ? BM->m_gu : B.m_gu,
                       BM ? BM->sgu : nullptr, g, s));
   }
+  if (rp) QI_TRY(probe(d, b, 6, d->h, static_cast<long long>(R) * kFfn, s));
   // down: x += g2 * (h Wd^T); xa = fp16(x (1 + s1)) for the next block
   {
     ProfScope ps(d, s, 4, b);
@@ -461,6 +481,7 @@ qi_status pass_embed(qi_dit* d, const PassRows& pr, const float* img, int N, con
     ProfScope ps(d, s, 5);
     if (pr.n_text > 0) {
       QI_CUDA(qi::launch_txt_prenorm(txt, L, d->txt_norm_w, d->txt_a, s));
+      QI_TRY(probe(d, 0, 7, d->txt_a, static_cast<long long>(L) * kHidden, s));
     }
     if (pr.n_img > 0) {
       const size_t off = static_cast<size_t>(pr.n_text);
@@ -1378,6 +1399,13 @@ qi_status qi_dit_set_trace(qi_dit* d, int slot, int block, float* dst) {
   if (dst && (block < 0 || block > d->blocks)) return fail(QI_ERR_INVALID_ARG, "qi_dit_set_trace: block %d", block);
   d->trace_block[slot] = dst ? block : -1;
   d->trace_dst[slot] = dst;
+  return QI_OK;
+}
+
+qi_status qi_dit_set_range_probe(qi_dit* d, float* out) {
+  if (!d) return fail(QI_ERR_INVALID_ARG, "qi_dit_set_range_probe: NULL handle");
+  if (out && (reinterpret_cast<uintptr_t>(out) & 3)) return fail(QI_ERR_INVALID_ARG, "qi_dit_set_range_probe: alignment");
+  d->range_out = out;
   return QI_OK;
 }
 

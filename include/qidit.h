@@ -440,6 +440,20 @@ qi_status qi_attention_f16(const uint16_t* q, const uint16_t* k, const uint16_t*
  * stream after the last block) into `dst` (device). slot 0 or 1; dst NULL clears. */
 qi_status qi_dit_set_trace(qi_dit* dit, int slot, int block, float* dst);
 
+/* fp16 operand ranges (test hook). The tensor-core operands are fp16, whose
+ * largest finite value is 65504; this records how close a pass comes to it.
+ * While `out` is set (device float32 [blocks][QI_RANGE_KINDS], filled with zeros
+ * by the caller), every later single-prompt pass of the fp16 mode folds, per
+ * block, the largest |value| of each fp16 operand it writes into out with an
+ * atomic max (a NaN counts as +inf). Kinds: 0 x (1 + s1), the Q/K/V GEMM's input;
+ * 1 Q after RoPE; 2 K after RoPE (the pass's rows of the block's K store); 3 V;
+ * 4 the attention output O; 5 x (1 + s2), the gate/up GEMM's input; 6 h, the
+ * SwiGLU output and down GEMM input; 7 the text projection's input (in block 0's
+ * row only). One extra reduction launch per operand; NULL turns it off.
+ * Errors: INVALID_ARG (NULL handle, misaligned out). */
+#define QI_RANGE_KINDS 8
+qi_status qi_dit_set_range_probe(qi_dit* dit, float* out);
+
 /* Per-kernel-class device time, measured with CUDA events on the launching
  * stream while enabled. Classes: 0 QKV GEMM, 1 attention, 2 out-proj GEMM,
  * 3 gate/up GEMM, 4 down GEMM, 5 other. Each timed launch group adds two event

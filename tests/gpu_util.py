@@ -56,3 +56,32 @@ def f16_tensor(a, device="cuda"):
 
 def f16_bits_to_f32(bits):
     return np.ascontiguousarray(bits).view(np.float16).astype(np.float32)
+
+
+FP16_MAX = 65504.0
+
+
+def check_ranges(dit_ranges, what):
+    """The largest |value| of every fp16 operand per block (qi_dit_set_range_probe) must be
+    finite and within fp16's range; the margins are written to $QI_RANGE_OUT (JSON lines)
+    when that variable is set. Returns the per-kind maxima over blocks."""
+    import json
+    import os
+
+    import diffusion_transformer_text_gb300 as qi
+    r = np.asarray(dit_ranges, np.float64)
+    assert np.isfinite(r).all() and (r < FP16_MAX).all(), f"{what}: fp16 operand range exceeded: {r.max(0)}"
+    per_kind = {k: float(r[:, i].max()) for i, k in enumerate(qi.RANGE_KINDS)}
+    path = os.environ.get("QI_RANGE_OUT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": what, "max_abs": per_kind,
+                                "margin_to_65504": {k: FP16_MAX / v if v > 0 else None for k, v in per_kind.items()}})
+                    + "\n")
+    return per_kind
+
+
+def range_buffer(dit):
+    import torch
+    import diffusion_transformer_text_gb300 as qi
+    return torch.zeros(dit.blocks, len(qi.RANGE_KINDS), dtype=torch.float32, device="cuda")

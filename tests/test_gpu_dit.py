@@ -6,7 +6,7 @@ import synth
 from oracle import dit as odit
 from oracle import rope as orope
 
-from gpu_util import assert_close, f16_bits_to_f32, f32_tensor, load_weights
+from gpu_util import assert_close, check_ranges, f16_bits_to_f32, f32_tensor, load_weights, range_buffer
 
 pytestmark = pytest.mark.gpu
 
@@ -104,11 +104,15 @@ def test_step_256(qi, dit256):
     img = synth.img_tokens(case)
     txt = synth.txt_feats(case)
     tc, ts, ic, is_ = _tables(case.L, case.h, case.w)
+    rb = range_buffer(d)
+    d.set_range_probe(rb)
     vel = d.step(f32_tensor(img), f32_tensor(txt), case.timestep, f32_tensor(tc), f32_tensor(ts), f32_tensor(ic),
                  f32_tensor(is_))
+    d.set_range_probe(None)
     d.check()
     ref = odit.dit_forward(W, img, txt, np.float32(case.timestep), tc, ts, ic, is_)
     assert_close(vel.cpu().numpy(), ref, "vel 256^2")
+    check_ranges(rb.cpu().numpy(), "256^2 joint step")
 
 
 def test_reuse_equals_joint_bit_exact(qi, dit256):
@@ -230,6 +234,55 @@ def test_nonfinite_velocity_is_reported(qi):
             d.check()
         assert e.value.status == 8
         d.check()  # the word was cleared by the report
+    finally:
+        d.close()
+
+
+def test_fp16_overflow_of_h_is_reported(qi):
+    """SwiGLU weights scaled by 128 (exact in bf16) push h far past fp16's 65504. The fp32
+    oracle shows the overflow is real and its velocity stays finite; the library, whose
+    down-GEMM input is fp16, must report QI_ERR_NONFINITE rather than return a finite
+    wrong velocity, and the range probe must see the overflow."""
+    case = synth.BLOCK_CASE
+    W = synth.Weights(seed=0, nblocks=1)
+    bw = dict(W.block(0))
+    for k in ("wg", "wu"):
+        bw[k] = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(bw[k]) * np.float32(128.0)).reshape(bw[k].shape)
+    W._blocks[0] = bw
+    img, txt = synth.img_tokens(case), synth.txt_feats(case)
+    tc, ts, ic, is_ = _tables(case.L, case.h, case.w)
+    t = np.float32(case.timestep)
+    # oracle: h of block 0 in fp32
+    R = case.L + case.N
+    mods = odit.row_mods(odit.modulation(W.glob, t), odit.modulation(W.glob, 0.0), case.L, R)
+    s1, g1, s2, g2 = odit.mod_chunks(mods)
+    cos, sin = np.concatenate([tc, ic]), np.concatenate([ts, is_])
+    x = odit.embed(W.glob, img, txt)
+    q, k, v = odit.block_qkv(bw, x, s1, cos, sin, 32)
+    from oracle.attention import attention_masked
+    o = attention_masked(q, k, v, case.L)
+    x1 = x + g1 * odit.linear(o.reshape(R, -1), bw["wo"])
+    xn2 = odit.rmsnorm(x1) * (np.float32(1.0) + s2)
+    h = odit.silu(odit.linear(xn2, bw["wg"])) * odit.linear(xn2, bw["wu"])
+    assert np.abs(h).max() > 4 * 65504.0
+    ref = odit.dit_forward(W, img, txt, t, tc, ts, ic, is_, nblocks=1)
+    assert np.isfinite(ref).all()
+    # library
+    d = qi.DiT(blocks=1, L_max=case.L, N_max=case.N)
+    try:
+        d.load_global(W.glob)
+        d.load_block(0, bw)
+        rb = range_buffer(d)
+        d.set_range_probe(rb)
+        d.step(f32_tensor(img), f32_tensor(txt), float(t), f32_tensor(tc), f32_tensor(ts), f32_tensor(ic),
+               f32_tensor(is_))
+        d.set_range_probe(None)
+        with pytest.raises(qi.QiError) as e:
+            d.check()
+        assert e.value.status == 8
+        r = rb.cpu().numpy()
+        assert np.isinf(r[0, qi.RANGE_KINDS.index("h")])
+        assert np.isfinite(r[0, :qi.RANGE_KINDS.index("h")]).all()
     finally:
         d.close()
 

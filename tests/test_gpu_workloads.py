@@ -21,7 +21,7 @@ from oracle import dit as odit
 from oracle import rope as orope
 from oracle import sched as osched
 
-from gpu_util import assert_close, f32_tensor, load_weights
+from gpu_util import assert_close, check_ranges, f32_tensor, load_weights, range_buffer
 
 pytestmark = pytest.mark.gpu
 
@@ -99,11 +99,21 @@ def test_384_two_prompts_reuse(qi):
             for i in range(5):
                 t = _t(ts, i)
                 if i == 0:
+                    rb = range_buffer(d)
+                    d.set_range_probe(rb)
                     vel = d.step(x, txt, t, tc, tsn, ic, isn).clone()
+                    d.set_range_probe(None)
+                    check_ranges(rb.cpu().numpy(), f"384^2 L={L} joint step 1")
                     ref = odit.dit_forward(W, x.cpu().numpy(), txt_np, np.float32(t), otc, ots, oic, ois)
                     assert_close(vel.cpu().numpy(), ref, f"384^2 L={L} step 1 vs oracle")
                 else:
+                    if i == 4:
+                        rb = range_buffer(d)
+                        d.set_range_probe(rb)
                     vel = d.step_cached(x, L, t, ic, isn).clone()
+                    if i == 4:
+                        d.set_range_probe(None)
+                        check_ranges(rb.cpu().numpy(), f"384^2 L={L} cached step 5")
                     joint = d.step(x, txt, t, tc, tsn, ic, isn)
                     assert np.array_equal(vel.cpu().numpy(), joint.cpu().numpy()), f"L={L} step {i + 1}"
                     if i == 4 and L == 494:
@@ -187,7 +197,11 @@ def test_1024_forty_step_loop(qi):
                 if i == 0:
                     _check_embed(W, tr.at(0, run), x_np, txt_np, rows_txt, rows_img, L, "1024^2 embedding")
                 x_fin = tr.at(32, run)
+                rb = range_buffer(d)
+                d.set_range_probe(rb)
                 vel = run().clone()
+                d.set_range_probe(None)
+                check_ranges(rb.cpu().numpy(), f"1024^2 step {i} ({'joint' if i == 0 else 'cached'})")
                 _check_head(W, x_fin[L:R] if i == 0 else x_fin[:N], vel.cpu().numpy(), rows_img,
                             f"1024^2 step {i} head")
                 if i > 0:
@@ -238,7 +252,11 @@ def test_2048_step(qi):
             _check_block(W, b, a_, b_[rows], mods, L, cos, sin, rows, f"2048^2 block {b}")
         _check_embed(W, tr.at(0, run), img_np, txt_np, rows_txt, rows_img, L, "2048^2 embedding")
         x_fin = tr.at(32, run)
+        rb = range_buffer(d)
+        d.set_range_probe(rb)
         vel = run().clone()
+        d.set_range_probe(None)
+        check_ranges(rb.cpu().numpy(), "2048^2 joint step")
         _check_head(W, x_fin[L:], vel.cpu().numpy(), rows_img, "2048^2 head")
         cached = d.step_cached(img, L, t, ic, isn)
         d.check()
