@@ -11,21 +11,23 @@
 // Work unit = 128 query rows of one head. A persistent grid (one CTA per SM)
 // walks the units head-major, so the CTAs running at one time share a few heads'
 // K/V in L2. Tensor memory (512 columns):
-//   [0,128) S buffer 0, [128,256) S buffer 1, [256,384) O, [384,448) and
-//   [448,512) two Q slots (fp16 pairs, the A operand of Q K^T).
+//   [0,128) O, [128,192) and [192,256) two Q slots (fp16 pairs, the A operand
+//   of Q K^T), [256,384) S, [384,448) and [448,512) two P buffers (fp16 pairs,
+//   the A operand of P V).
 // Q sits in tensor memory, so Q K^T reads only K from shared memory (shared
 // memory bandwidth, not the tensor core, is what a second operand stream from
-// shared memory would saturate). P overwrites the first 64 columns of its S
-// buffer as fp16 pairs and is the A operand of P V.
+// shared memory would saturate). P has buffers of its own, so S(j+1) only
+// waits for the softmax warps to have read S(j) into registers, not for
+// P(j) V(j): the Q K^T of the next tile runs under the softmax of this one.
 //
 // Two threads issue the MMAs: one Q K^T, one P V. A thread issuing an N = 128
 // MMA is held about as long as the MMA runs, and each of its barrier checks
 // leaves the tensor pipe idle, so with a single issuer the pipe ran dry between
-// groups; with two, one thread's waits overlap the other's MMAs. S(j+2) waits
-// for P(j) V(j) (P shares S buffer j % 2); P(j) V(j) waits for the softmax of
-// tile j. Across units nothing drains: the next unit's Q is loaded into the
-// other Q slot during the current unit, its Q K^T start as soon as the S
-// buffers free, and only its first P V waits for the epilogue to have read O.
+// groups; with two, one thread's waits overlap the other's MMAs. P(j) V(j)
+// waits for the softmax of tile j; the softmax writes P(j) once P(j-2) V(j-2)
+// has read that buffer. Across units nothing drains: the next unit's Q is
+// loaded into the other Q slot during the current unit, its Q K^T start as
+// soon as S is read, and only its first P V waits for the epilogue to have read O.
 //
 // Roles (512 threads, four warpgroups):
 //   warp 0      TMA producer of the K tiles (ring of 3); warp 2 of the V tiles
@@ -62,8 +64,10 @@ constexpr int kBox = 128 * 64 * 2;             // 128 rows x 64 dims: one 128-by
 constexpr int kTile = 2 * kBox;                // K or V tile: 128 keys x 128 dims (32 KB)
 constexpr int kStages = 3;                     // depth of the K ring and of the V ring
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;
-constexpr uint32_t kColQ = 384;
+constexpr uint32_t kColO = 0;
+constexpr uint32_t kColQ = 128;
+constexpr uint32_t kColS = 256;
+constexpr uint32_t kColP = 384;
 constexpr uint32_t kIdescQK = idesc_f16_f32(128, kBKV);      // A = Q (tensor memory), B = K (K-major)
 constexpr uint32_t kIdescPV = idesc_f16_f32_bmn(128, 128);   // A = P (tensor memory), B = V (MN-major)
 constexpr float kRescaleLog2 = 8.0f;           // rescale O only when the max grows by > 2^8
@@ -77,8 +81,9 @@ enum : int {
   kKEmpty = kKFull + kStages,
   kVFull = kKEmpty + kStages,
   kVEmpty = kVFull + kStages,
-  kSFull = kVEmpty + kStages,  // [2] S buffer written
-  kPFull = kSFull + 2,         // [2] P written (8 softmax warps)
+  kSFull = kVEmpty + kStages,  // S written
+  kSFree = kSFull + 1,         // S read into registers (8 softmax warps)
+  kPFull = kSFree + 1,         // [2] P buffer written (8 softmax warps)
   kPvDone = kPFull + 2,        // [2] P V of the buffer's tile complete
   kQFull = kPvDone + 2,        // [2] Q slot loaded (4 epilogue warps)
   kQEmpty = kQFull + 2,        // [2] last Q K^T of the slot's unit complete
@@ -114,7 +119,7 @@ __device__ __forceinline__ bool mbar_count4(int i) {
   return (i >= kQFull && i < kQFull + 2) || i == kOEmpty;
 }
 __device__ __forceinline__ bool mbar_count8(int i) {
-  return (i >= kPFull && i < kPFull + 2) || (i >= kLFull && i < kLFull + 2);
+  return i == kSFree || (i >= kPFull && i < kPFull + 2) || (i >= kLFull && i < kLFull + 2);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -193,8 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t i = t > kStages ? t - kStages : 0; i < t; ++i)
         if (!mbar_wait(&full[i % kStages], (i / kStages) & 1u)) report_error(p.err, kErrTimeoutDrain);
     } else if (warp == 1) {
-      // ---------------- Q K^T issuer: S(tt) = Q K(tt)^T into S buffer tt % 2, once
-      // P V of tile tt - 2 (which read P from that buffer) has completed
+      // ---------------- Q K^T issuer: S(t) = Q K(t)^T, once the softmax warps have
+      // read S(t - 1)
       // descriptor of stage 0's K tile; the others differ in the start address field
       const uint64_t kdesc0 = sw128_kmajor_desc(smem_u32(sK));
       uint32_t t = 0;
@@ -208,18 +213,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t tQ = tmem + kColQ + qs * 64;
         for (int j = 0; j < un.ntiles; ++j, ++t) {
-          const uint32_t b = t & 1u;
           const uint32_t st = t % kStages;
-          ok = (t < 2 || mbar_wait(&bars[kPvDone + b], ((t - 2) >> 1) & 1u)) &&
-               mbar_wait(&bars[kKFull + st], (t / kStages) & 1u);
+          ok = (t < 1 || mbar_wait(&bars[kSFree], (t - 1) & 1u)) && mbar_wait(&bars[kKFull + st], (t / kStages) & 1u);
           if (!ok) break;
           tc_fence_after();
           const uint64_t kd = kdesc0 + ((st * kTile) >> 4);
 #pragma unroll
           for (int k = 0; k < kHeadDim / 16; ++k)
-            mma_ts(tmem + b * kBKV, tQ + k * 8, kd + (((k >> 2) * kBox + (k & 3) * 32) >> 4), kIdescQK,
+            mma_ts(tmem + kColS, tQ + k * 8, kd + (((k >> 2) * kBox + (k & 3) * 32) >> 4), kIdescQK,
                    k > 0 ? 1u : 0u);
-          mma_commit(&bars[kSFull + b]);
+          mma_commit(&bars[kSFull]);
           mma_commit(&bars[kKEmpty + st]);
         }
         if (!ok) break;
@@ -257,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kBKV / 16; ++k)
             // P columns: 16 keys = 8 columns of fp16 pairs; V rows: 16 keys = 2 KB
-            mma_ts(tmem + kColO, tmem + b * kBKV + k * 8, vd + ((k * 2048) >> 4), kIdescPV,
+            mma_ts(tmem + kColO, tmem + kColP + b * 64 + k * 8, vd + ((k * 2048) >> 4), kIdescPV,
                    (j > 0 || k > 0) ? 1u : 0u);
           mma_commit(&bars[kPvDone + b]);
           mma_commit(&bars[kVEmpty + st]);
@@ -293,15 +296,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < un.ntiles; ++j) {
         const uint32_t tt = t + j;
         const uint32_t b = tt & 1u;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars[kSFull + b], (tt >> 1) & 1u));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars[kSFull], tt & 1u));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t tS = tmem + lane_off + b * kBKV;
-        // this half's 64 S columns: two loads in flight, one wait
+        const uint32_t tS = tmem + lane_off + kColS;
+        // this half's 64 S columns: two loads in flight, one wait; then S may be
+        // overwritten by the next tile's Q K^T
         uint32_t r[2][32];
         tmem_ld32(tS + h * 64, r[0]);
         tmem_ld32(tS + h * 64 + 32, r[1]);
         tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kSFree]);
         // keys at or past the row's limit become -inf (only tiles that reach a limit)
         const int kbase = j * kBKV + h * 64;
         if (__any_sync(0xffffffffu, kbase + 64 > lim)) {
@@ -317,11 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; i += 2)
             mx4[(i >> 1) & 3] = fmax3(mx4[(i >> 1) & 3], __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
-        // swap half maxima with the warp that holds the row's other half; after the
-        // swap both halves have read their S columns, so P may overwrite them
+        // swap half maxima with the warp that holds the row's other half
         float* hm = hmax + (tt & 1u) * 2 * kBQ;
         hm[h * kBQ + rit] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        tc_fence_before();
         __syncwarp();
         uint64_t* xb = &bars[kXchg + (tt & 1u) * 4 + quarter];
         if (lane == 0) mbar_arrive(xb);
@@ -366,7 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // P = 2^(s * scale - m) as fp16 pairs: this half's 64 keys go to columns
-        // 32 h .. 32 h + 31 of the S buffer (masked keys give 2^-inf = 0)
+        // 32 h .. 32 h + 31 of P buffer tt % 2 (masked keys give 2^-inf = 0), once
+        // P V of tile tt - 2 has read that buffer
+        if (tt >= 2) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars[kPvDone + b], ((tt - 2) >> 1) & 1u));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const uint32_t tP = tmem + lane_off + kColP + b * 64;
         const uint64_t nm2 = f2_pack(-m_used, -m_used);
         uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
@@ -383,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             rs2[i & 3] = add_f32x2(rs2[i & 3], f2_pack(e0, e1));
             pk[i] = pack_f16x2(e0, e1);
           }
-          tmem_st16(tS + h * 32 + c * 16, pk);
+          tmem_st16(tP + h * 32 + c * 16, pk);
         }
         float s[8];
 #pragma unroll
