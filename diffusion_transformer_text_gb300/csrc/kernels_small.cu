@@ -34,56 +34,84 @@ __global__ void timestep_embed_kernel(float t, float* e) {
 }
 
 // y[r][o] = W[o] . act(x[r]) + b[o] for r = 0, 1; act = silu or identity.
-// Each warp computes kOutPerWarp outputs; W rows are read once, 16 bytes per lane.
+// Each warp computes kOutPerWarp outputs at a time; W rows are read once, 16 bytes
+// per lane. The grid is a multiple of the SM count and output group g goes to
+// block g % gridDim.x, so every SM streams the same share of W (a grid of whole
+// 32-output blocks left some SMs a quarter more than others); the first chunk of
+// a warp's rows is requested before x is staged in shared memory.
 constexpr int kOutPerWarp = 4;
 __global__ void __launch_bounds__(256) gemv2_kernel(const float* __restrict__ x, int in_dim,
                                                     const uint16_t* __restrict__ W, const uint16_t* __restrict__ b,
                                                     int out_dim, float* __restrict__ y, int silu_in) {
   extern __shared__ float xs[];  // [2][in_dim]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warps_total = gridDim.x * (blockDim.x >> 5);
+  const int groups = (out_dim + kOutPerWarp - 1) / kOutPerWarp;
+  const int chunks = in_dim / 8;
+  int grp = blockIdx.x + warp * gridDim.x;
+  const uint4* wr[kOutPerWarp];
+  auto rows_of = [&](int gi) {
+#pragma unroll
+    for (int j = 0; j < kOutPerWarp; ++j)
+      wr[j] = reinterpret_cast<const uint4*>(W + static_cast<size_t>(min(gi * kOutPerWarp + j, out_dim - 1)) * in_dim);
+  };
+  uint4 wv[kOutPerWarp];
+  if (grp < groups) {
+    rows_of(grp);
+    if (lane < chunks) {
+#pragma unroll
+      for (int j = 0; j < kOutPerWarp; ++j) wv[j] = wr[j][lane];
+    }
+  }
   for (int i = threadIdx.x; i < 2 * in_dim; i += blockDim.x) {
     const float v = x[i];
     xs[i] = silu_in ? silu(v) : v;
   }
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int o_base = (blockIdx.x * 8 + warp) * kOutPerWarp;
-  const int chunks = in_dim / 8;
-  // the warp's rows side by side, so each lane has a 16-byte load of every row in
-  // flight; each row's per-lane sum runs over c in the same order as alone
-  const uint4* wr[kOutPerWarp];
+  for (; grp < groups; grp += warps_total) {
+    const int o_base = grp * kOutPerWarp;
+    // the warp's rows side by side, so each lane has a 16-byte load of every row in
+    // flight; each row's per-lane sum runs over c in the same order as alone
+    float a0[kOutPerWarp], a1[kOutPerWarp];
 #pragma unroll
-  for (int j = 0; j < kOutPerWarp; ++j)
-    wr[j] = reinterpret_cast<const uint4*>(W + static_cast<size_t>(min(o_base + j, out_dim - 1)) * in_dim);
-  float a0[kOutPerWarp], a1[kOutPerWarp];
+    for (int j = 0; j < kOutPerWarp; ++j) a0[j] = a1[j] = 0.f;
+    for (int c = lane; c < chunks; c += 32) {
+      if (c != lane) {
 #pragma unroll
-  for (int j = 0; j < kOutPerWarp; ++j) a0[j] = a1[j] = 0.f;
-  for (int c = lane; c < chunks; c += 32) {
-    uint4 wv[kOutPerWarp];
+        for (int j = 0; j < kOutPerWarp; ++j) wv[j] = wr[j][c];
+      }
+      const float* x0 = xs + c * 8;
+      const float* x1 = xs + in_dim + c * 8;
 #pragma unroll
-    for (int j = 0; j < kOutPerWarp; ++j) wv[j] = wr[j][c];
-    const float* x0 = xs + c * 8;
-    const float* x1 = xs + in_dim + c * 8;
+      for (int j = 0; j < kOutPerWarp; ++j) {
+        const uint32_t ws[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
 #pragma unroll
-    for (int j = 0; j < kOutPerWarp; ++j) {
-      const uint32_t ws[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float lo = __uint_as_float(ws[q] << 16);
-        const float hi = __uint_as_float(ws[q] & 0xFFFF0000u);
-        a0[j] += lo * x0[2 * q] + hi * x0[2 * q + 1];
-        a1[j] += lo * x1[2 * q] + hi * x1[2 * q + 1];
+        for (int q = 0; q < 4; ++q) {
+          const float lo = __uint_as_float(ws[q] << 16);
+          const float hi = __uint_as_float(ws[q] & 0xFFFF0000u);
+          a0[j] += lo * x0[2 * q] + hi * x0[2 * q + 1];
+          a1[j] += lo * x1[2 * q] + hi * x1[2 * q + 1];
+        }
       }
     }
-  }
 #pragma unroll
-  for (int j = 0; j < kOutPerWarp; ++j) {
-    const int o = o_base + j;
-    const float s0 = warp_sum(a0[j]);
-    const float s1 = warp_sum(a1[j]);
-    if (lane == 0 && o < out_dim) {
-      const float bb = bf16_bits_to_float(b[o]);
-      y[o] = s0 + bb;
-      y[out_dim + o] = s1 + bb;
+    for (int j = 0; j < kOutPerWarp; ++j) {
+      const int o = o_base + j;
+      const float s0 = warp_sum(a0[j]);
+      const float s1 = warp_sum(a1[j]);
+      if (lane == 0 && o < out_dim) {
+        const float bb = bf16_bits_to_float(b[o]);
+        y[o] = s0 + bb;
+        y[out_dim + o] = s1 + bb;
+      }
+    }
+    // the next group's first chunk
+    if (grp + warps_total < groups) {
+      rows_of(grp + warps_total);
+      if (lane < chunks) {
+#pragma unroll
+        for (int j = 0; j < kOutPerWarp; ++j) wv[j] = wr[j][lane];
+      }
     }
   }
 }
@@ -638,14 +666,20 @@ cudaError_t launch_timestep_embed(float t, float* e, cudaStream_t s) {
 
 cudaError_t launch_gemv2(const float* x, int in_dim, const uint16_t* W, const uint16_t* b, int out_dim, float* y,
                          int silu_in, cudaStream_t s) {
-  const int per_block = 8 * kOutPerWarp;
   const size_t smem = 2 * static_cast<size_t>(in_dim) * sizeof(float);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(gemv2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  gemv2_kernel<<<(out_dim + per_block - 1) / per_block, 256, smem, s>>>(x, in_dim, W, b, out_dim, y, silu_in);
+  // four blocks of 8 warps per SM (or fewer if there are fewer output groups)
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int groups = (out_dim + kOutPerWarp - 1) / kOutPerWarp;
+  const int grid = groups < 4 * sms ? groups : 4 * sms;
+  gemv2_kernel<<<grid, 256, smem, s>>>(x, in_dim, W, b, out_dim, y, silu_in);
   return cudaGetLastError();
 }
 
