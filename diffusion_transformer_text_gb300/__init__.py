@@ -39,7 +39,7 @@ SYMBOLS = (
     "qi_rope_axis_tables", "qi_rope_tables", "qi_flow_sigmas", "qi_pack_noise", "qi_euler_update",
     "qi_dit_step", "qi_text_kv_capture", "qi_kv_cache_bytes", "qi_dit_check",
     "qi_dit_block_forward", "qi_dit_read_kv", "qi_dit_set_trace", "qi_dit_profile", "qi_dit_profile_classes",
-    "qi_dit_profile_read", "qi_last_error", "qi_gemm_bf16", "qi_attention_f16", "qi_gemm_bf16_noalloc",
+    "qi_dit_profile_read", "qi_last_error", "qi_gemm_bf16", "qi_attention_f16", "qi_gemm_bf16_noalloc", "qi_gemv_bf16",
     "qi_dit_step_cfg", "qi_dpmpp2m_coeffs", "qi_dpmpp2m_update", "qi_dit_step_fbcache", "qi_dit_fbcache_reset",
     "qi_dit_set_mxfp8", "qi_quant_mxfp8", "qi_gemm_mxfp8", "qi_debug_inject", "qi_dit_euler_step", "qi_dit_set_range_probe",
 )
@@ -110,6 +110,7 @@ def lib() -> ctypes.CDLL:
         "qi_dit_profile_read": [P, P, P],
         "qi_gemm_bf16": [P, P, P, P, I, I, I, P],
         "qi_attention_f16": [P, P, P, P, I, I, I, I, P],
+        "qi_gemv_bf16": [P, I, P, P, I, P, I, P],
         "qi_gemm_bf16_noalloc": [P, P, P, I, I, I, I, P],
         "qi_dit_step_cfg": [P, P, I, F, F, P, I, P, P, P, P, P, I, P, P, P, P, P, U, P],
         "qi_dpmpp2m_coeffs": [P, I, I, P, P],
@@ -268,6 +269,16 @@ def attention(q, k, v, L: int, q_off: int = 0, Lk: int | None = None):
     o = torch.empty(Rq, HIDDEN, dtype=q.dtype, device=q.device)
     _check(lib().qi_attention_f16(_ptr(q), _ptr(k), _ptr(v), _ptr(o), Rq, q_off, L, Lk, _stream()))
     return o
+
+
+def gemv(x, W, b, silu_in: bool = False):
+    """Test hook: the two-row GEMV of the timestep MLP and the shared modulation.
+    x fp32 [2, in_dim], W bf16 bits [out_dim, in_dim], b bf16 bits [out_dim] -> y fp32 [2, out_dim]."""
+    import torch
+    out_dim, in_dim = W.shape
+    y = torch.empty(2, out_dim, dtype=torch.float32, device=x.device)
+    _check(lib().qi_gemv_bf16(_ptr(x), in_dim, _ptr(W), _ptr(b), out_dim, _ptr(y), int(silu_in), _stream()))
+    return y
 
 
 # ---------------------------------------------------------------- the DiT

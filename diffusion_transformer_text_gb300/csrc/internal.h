@@ -188,8 +188,14 @@ bool encode_map16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols
 
 // Small kernels (kernels_small.cu)
 cudaError_t launch_timestep_embed(float t, float* e, cudaStream_t s);
+// y[r][o] = W[o] . act(x[r]) + b[o], r = 0, 1 (x [2][in_dim] fp32, W [out_dim][in_dim]
+// bf16, act = silu if silu_in); in_dim = 4096 takes the streamed kernel (W and x
+// 16-byte aligned), which reports a bounded wait's expiry in `err` (may be null).
+// weights_preloaded: W was complete before the previous kernel in the stream began
+// (the handle's weight store, written by copies at load), so the streamed kernel
+// is launched dependent on that kernel and starts reading W while it finishes.
 cudaError_t launch_gemv2(const float* x, int in_dim, const uint16_t* W, const uint16_t* b, int out_dim, float* y,
-                         int silu_in, cudaStream_t s);
+                         int silu_in, int* err, bool weights_preloaded, cudaStream_t s);
 cudaError_t launch_txt_prenorm(const float* txt, int L, const uint16_t* w, act_t* out, cudaStream_t s);
 cudaError_t launch_img_in(const float* img, int N, const uint16_t* W, const uint16_t* b, const float* mod,
                           float* x, act_t* xa, float* ssp, cudaStream_t s);

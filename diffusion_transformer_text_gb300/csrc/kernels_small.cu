@@ -116,6 +116,176 @@ __global__ void __launch_bounds__(256) gemv2_kernel(const float* __restrict__ x,
   }
 }
 
+// The same product for 4096-wide rows, streamed. One CTA per SM takes a
+// contiguous range of W rows (8 KB each); a producer warp bulk-copies them into a
+// ring of kGvStages stages of kGvRows rows, so every SM keeps ~192 KB of its share
+// of W in flight (per-warp loads left too little in flight to reach the copy
+// rate). Eight consumer warps never wait for one another: thread t holds act(x) at
+// elements 8 t .. 8 t + 7 and 2048 + 8 t .. 2048 + 8 t + 7 of both rows in
+// registers and multiplies the same elements of every W row; each warp sums its
+// lanes' products of a stage (a butterfly that leaves one of the stage's 8 sums
+// on each group of 4 lanes), parks them in shared memory and releases the stage.
+// At the end the 8 warps' sums of every output are added in warp order, so an
+// output is summed the same way on every call.
+constexpr int kGvIn = 4096;
+constexpr int kGvRows = 4;                                  // W rows per stage
+constexpr int kGvStageBytes = kGvRows * kGvIn * 2;         // 32 KB
+constexpr int kGvStages = 6;
+constexpr int kGvWarps = 8;                                 // consumer warps
+constexpr int kGvThreads = 32 * (kGvWarps + 1);             // + the producer warp
+constexpr int kGvMaxRows = 128;                             // W rows per CTA at most
+constexpr int kGvSmem = kGvStages * kGvStageBytes + 2 * kGvStages * 8 + kGvWarps * kGvMaxRows * 2 * 4 + 16;
+
+__global__ void __launch_bounds__(kGvThreads, 1)
+    gemv_stream_kernel(const float* __restrict__ x, const uint16_t* __restrict__ W, const uint16_t* __restrict__ b,
+                       int out_dim, float* __restrict__ y, int silu_in, int* err) {
+  extern __shared__ __align__(128) uint8_t gv_smem[];
+  uint8_t* ring = gv_smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(gv_smem + kGvStages * kGvStageBytes);
+  uint64_t* empty = full + kGvStages;
+  float* part = reinterpret_cast<float*>(empty + kGvStages);  // [warp][row][2]
+  volatile int* failed = reinterpret_cast<volatile int*>(part + kGvWarps * kGvMaxRows * 2);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r_begin = static_cast<int>(static_cast<long long>(out_dim) * blockIdx.x / gridDim.x);
+  const int r_end = static_cast<int>(static_cast<long long>(out_dim) * (blockIdx.x + 1) / gridDim.x);
+  const int nrows = r_end - r_begin;  // <= kGvMaxRows (the launcher's grid)
+  const int ngroups = (nrows + kGvRows - 1) / kGvRows;
+  if (tid == 0) {
+    for (int i = 0; i < kGvStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kGvWarps);
+    }
+    *failed = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  grid_dep_launch_dependents();
+  // Launched dependent on the previous kernel (a step's timestep and modulation
+  // GEMVs), the W stream starts at once: the weights are written only by copies
+  // when they are loaded. x is read, and y written, after the previous kernel.
+  if (warp == kGvWarps) {
+    // ---------------- producer: group gi into stage gi % kGvStages once every
+    // consumer warp has released the stage's previous group
+    if (lane == 0) {
+      int gi = 0;
+      for (; gi < ngroups; ++gi) {
+        const int st = gi % kGvStages;
+        if (gi >= kGvStages && !mbar_wait(&empty[st], static_cast<uint32_t>(gi / kGvStages - 1) & 1u)) {
+          report_error(err, kErrTimeoutProducer);
+          *failed = 1;
+          break;
+        }
+        fence_proxy_async_smem();
+        // the group's rows are consecutive in W: one copy
+        const int r0 = r_begin + gi * kGvRows;
+        const uint32_t bytes = static_cast<uint32_t>(min(kGvRows, r_end - r0)) * kGvIn * 2;
+        mbar_arrive_expect_tx(&full[st], bytes);
+        bulk_load(ring + st * kGvStageBytes, W + static_cast<size_t>(r0) * kGvIn, bytes, &full[st]);
+      }
+      // the last stages' copies must land before the CTA exits
+      for (int g2 = gi > kGvStages ? gi - kGvStages : 0; g2 < gi; ++g2)
+        if (!mbar_wait(&full[g2 % kGvStages], static_cast<uint32_t>(g2 / kGvStages) & 1u)) {
+          report_error(err, kErrTimeoutDrain);
+          break;
+        }
+    }
+  } else {
+    // ---------------- consumers
+    grid_dep_wait();
+    float xa[2][16];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float4* src = reinterpret_cast<const float4*>(x + r * kGvIn + h * 2048 + 8 * tid);
+        const float4 v0 = src[0], v1 = src[1];
+        const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xa[r][h * 8 + i] = silu_in ? silu(v[i]) : v[i];
+      }
+    // after the butterfly, lanes 4 k .. 4 k + 3 hold sum number
+    // (bit 4 of the lane) * 4 + (bit 3) * 2 + (bit 2) = row * 2 + x-row
+    const int my_sum = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+    for (int gi = 0; gi < ngroups; ++gi) {
+      const int st = gi % kGvStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[st], static_cast<uint32_t>(gi / kGvStages) & 1u))) {
+        if (lane == 0) {
+          report_error(err, kErrTimeoutEpilogue);
+          *failed = 1;
+        }
+        break;
+      }
+      const int n = min(kGvRows, nrows - gi * kGvRows);
+      const uint4* wst = reinterpret_cast<const uint4*>(ring + st * kGvStageBytes);
+      float v[2 * kGvRows];
+#pragma unroll
+      for (int i = 0; i < kGvRows; ++i) {
+        float a0 = 0.f, a1 = 0.f;
+        if (i < n) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint4 w = wst[i * (kGvIn / 8) + h * 256 + tid];
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float lo = __uint_as_float(ws[q] << 16);
+              const float hi = __uint_as_float(ws[q] & 0xFFFF0000u);
+              a0 = fmaf(hi, xa[0][h * 8 + 2 * q + 1], fmaf(lo, xa[0][h * 8 + 2 * q], a0));
+              a1 = fmaf(hi, xa[1][h * 8 + 2 * q + 1], fmaf(lo, xa[1][h * 8 + 2 * q], a1));
+            }
+          }
+        }
+        v[2 * i] = a0;
+        v[2 * i + 1] = a1;
+      }
+      // the stage is in registers: release it
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+      // butterfly: at distance 16 each lane keeps half of the 8 sums (adding its
+      // partner's copy of them) and hands over the other half; then 8 and 4; then a
+      // plain sum over distances 2 and 1
+      float w4[4], w2[2];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const bool up = (lane & 16) != 0;
+        const float give = up ? v[i] : v[i + 4];
+        const float keep = up ? v[i + 4] : v[i];
+        w4[i] = keep + __shfl_xor_sync(0xffffffffu, give, 16);
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const bool up = (lane & 8) != 0;
+        const float give = up ? w4[i] : w4[i + 2];
+        const float keep = up ? w4[i + 2] : w4[i];
+        w2[i] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
+      }
+      float w1;
+      {
+        const bool up = (lane & 4) != 0;
+        const float give = up ? w2[0] : w2[1];
+        const float keep = up ? w2[1] : w2[0];
+        w1 = keep + __shfl_xor_sync(0xffffffffu, give, 4);
+      }
+      w1 += __shfl_xor_sync(0xffffffffu, w1, 2);
+      w1 += __shfl_xor_sync(0xffffffffu, w1, 1);
+      if ((lane & 3) == 0 && (my_sum >> 1) < n)
+        part[(warp * kGvMaxRows + gi * kGvRows + (my_sum >> 1)) * 2 + (my_sum & 1)] = w1;
+    }
+  }
+  __syncthreads();
+  if (*failed) return;
+  grid_dep_wait();
+  // every output of the CTA: its 8 warp sums in warp order, plus the bias
+  for (int k = tid; k < 2 * nrows; k += kGvThreads) {
+    const int row = k >> 1, r = k & 1;
+    float sum = 0.f;
+#pragma unroll
+    for (int w2 = 0; w2 < kGvWarps; ++w2) sum += part[(w2 * kGvMaxRows + row) * 2 + r];
+    const int o = r_begin + row;
+    y[r * out_dim + o] = sum + bf16_bits_to_float(b[o]);
+  }
+}
+
 // ---------------------------------------------------------------- norms
 
 __device__ __forceinline__ float block_sum_256(float v, float* red) {
@@ -665,7 +835,29 @@ cudaError_t launch_timestep_embed(float t, float* e, cudaStream_t s) {
 }
 
 cudaError_t launch_gemv2(const float* x, int in_dim, const uint16_t* W, const uint16_t* b, int out_dim, float* y,
-                         int silu_in, cudaStream_t s) {
+                         int silu_in, int* err, bool weights_preloaded, cudaStream_t s) {
+  if (out_dim <= 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (in_dim == kGvIn) {
+    // bulk copies and vector loads need 16-byte aligned W and x
+    if ((reinterpret_cast<uintptr_t>(W) & 15) != 0 || (reinterpret_cast<uintptr_t>(x) & 15) != 0)
+      return cudaErrorInvalidValue;
+    static std::atomic<unsigned long long> attr_done{0};
+    e = ensure_smem_limit(gemv_stream_kernel, kGvSmem, attr_done);
+    if (e != cudaSuccess) return e;
+    // one CTA per SM, or more so that no CTA has more than kGvMaxRows rows
+    int grid = out_dim < sms ? out_dim : sms;
+    const int need = (out_dim + kGvMaxRows - 1) / kGvMaxRows;
+    if (grid < need) grid = need;
+    if (weights_preloaded)
+      return launch_dependent(gemv_stream_kernel, dim3(grid), dim3(kGvThreads), kGvSmem, s, x, W, b, out_dim, y,
+                              silu_in, err);
+    gemv_stream_kernel<<<grid, kGvThreads, kGvSmem, s>>>(x, W, b, out_dim, y, silu_in, err);
+    return cudaGetLastError();
+  }
   const size_t smem = 2 * static_cast<size_t>(in_dim) * sizeof(float);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(gemv2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -673,10 +865,6 @@ cudaError_t launch_gemv2(const float* x, int in_dim, const uint16_t* W, const ui
     if (e != cudaSuccess) return e;
   }
   // four blocks of 8 warps per SM (or fewer if there are fewer output groups)
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
   const int groups = (out_dim + kOutPerWarp - 1) / kOutPerWarp;
   const int grid = groups < 4 * sms ? groups : 4 * sms;
   gemv2_kernel<<<grid, 256, smem, s>>>(x, in_dim, W, b, out_dim, y, silu_in);

@@ -114,6 +114,13 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
+// Orders this thread's earlier generic-proxy shared-memory accesses (and those
+// of the threads it synchronised with) before its later async-proxy ones, e.g. a
+// bulk copy into a buffer the CTA has just finished reading.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ dependent launch
 //
 // A kernel launched with programmatic stream serialization may start while the

@@ -269,9 +269,9 @@ qi_status probe(qi_dit* d, int block, int kind, const act_t* a, long long n, cud
 qi_status compute_mod(qi_dit* d, float t, cudaStream_t s) {
   ProfScope ps(d, s, 5);
   QI_CUDA(qi::launch_timestep_embed(t, d->temb_e, s));
-  QI_CUDA(qi::launch_gemv2(d->temb_e, kTdim, d->t_w1, d->t_b1, kHidden, d->temb_h, 0, s));
-  QI_CUDA(qi::launch_gemv2(d->temb_h, kHidden, d->t_w2, d->t_b2, kHidden, d->temb, 1, s));
-  QI_CUDA(qi::launch_gemv2(d->temb, kHidden, d->mod_w, d->mod_b, kMod, d->mod, 1, s));
+  QI_CUDA(qi::launch_gemv2(d->temb_e, kTdim, d->t_w1, d->t_b1, kHidden, d->temb_h, 0, d->err, true, s));
+  QI_CUDA(qi::launch_gemv2(d->temb_h, kHidden, d->t_w2, d->t_b2, kHidden, d->temb, 1, d->err, true, s));
+  QI_CUDA(qi::launch_gemv2(d->temb, kHidden, d->mod_w, d->mod_b, kMod, d->mod, 1, d->err, true, s));
   return QI_OK;
 }
 
@@ -1391,6 +1391,16 @@ qi_status qi_attention_f16(const uint16_t* q, const uint16_t* k, const uint16_t*
   a.L = L;
   a.Lk = Lk;
   QI_CUDA(qi::launch_attention(a, reinterpret_cast<cudaStream_t>(stream)));
+  return QI_OK;
+}
+
+qi_status qi_gemv_bf16(const float* x, int in_dim, const uint16_t* W, const uint16_t* b, int out_dim, float* y,
+                       int silu_in, qi_stream_t stream) {
+  if (!x || !W || !b || !y) return fail(QI_ERR_INVALID_ARG, "qi_gemv_bf16: NULL argument");
+  if (out_dim < 1 || (in_dim != kTdim && in_dim != kHidden))
+    return fail(QI_ERR_SHAPE, "qi_gemv_bf16: in_dim %d (256 or 4096) out_dim %d", in_dim, out_dim);
+  QI_CUDA(qi::launch_gemv2(x, in_dim, W, b, out_dim, y, silu_in ? 1 : 0, nullptr, false,
+                           reinterpret_cast<cudaStream_t>(stream)));
   return QI_OK;
 }
 

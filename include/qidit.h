@@ -435,6 +435,17 @@ qi_status qi_gemm_bf16_noalloc(const uint16_t* A, const uint16_t* B, float* D, i
 qi_status qi_attention_f16(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, int Rq,
                             int q_off, int L, int Lk, qi_stream_t stream);
 
+/* The two-row GEMV of the timestep MLP and the shared modulation on its own (test
+ * hook; Core AI page, architecture table: the modulation Linear 4096 -> 16384
+ * shared by all blocks, with a row for the sampled t and a row for t = 0):
+ * y[r][o] = W[o] . act(x[r]) + b[o] for r = 0, 1, act = SiLU if silu_in else the
+ * identity. x float32 [2, in_dim], W bf16 bits [out_dim, in_dim] row-major, b bf16
+ * bits [out_dim], y float32 [2, out_dim], all device; in_dim is 256 or 4096
+ * (else QI_ERR_SHAPE), x and W 16-byte aligned when in_dim = 4096. The caller owns
+ * every buffer; the call only enqueues on `stream`. */
+qi_status qi_gemv_bf16(const float* x, int in_dim, const uint16_t* W, const uint16_t* b, int out_dim, float* y,
+                       int silu_in, qi_stream_t stream);
+
 /* During later qi_dit_step calls, copy the float32 residual stream entering
  * block `block` ([R, 4096], R = rows of that pass; `block` = blocks means the
  * stream after the last block) into `dst` (device). slot 0 or 1; dst NULL clears. */

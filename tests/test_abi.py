@@ -95,6 +95,7 @@ def test_status_codes(qi):
     assert L.qi_euler_update(None, None, 8, 1.0, 0.5, None) == 1
     assert L.qi_dit_step(None, None, 8, None, 8, 0.5, None, None, None, None, None, 0, None) == 1
     assert L.qi_attention_f16(None, None, None, None, 1, 0, 1, 1, None) == 1
+    assert L.qi_gemv_bf16(None, 4096, None, None, 16, None, 0, None) == 1
     assert L.qi_dit_profile(None, 1) == 1
     assert L.qi_dit_profile_classes(None, 8, 1) == 1
 

@@ -30,6 +30,31 @@ def small_dit(qi):
     d.close()
 
 
+# ---------------------------------------------------------------- GEMV
+
+@pytest.mark.parametrize("in_dim,out_dim,silu_in", [(4096, 16384, True), (4096, 4096, True), (4096, 1000, False),
+                                                    (4096, 100, True), (256, 4096, False)])
+def test_gemv_matches_product(qi, in_dim, out_dim, silu_in):
+    """The timestep / modulation GEMV (Core AI page, architecture table) against the
+    float64 product of its bf16 weights and the oracle's activation, twice in a row
+    (the streamed kernel's barriers start each call from phase 0); out_dim = 1000
+    gives CTAs a partial last group of rows, out_dim = 100 fewer rows than SMs."""
+    from oracle import dit as odit
+    rng = np.random.default_rng(in_dim + out_dim)
+    x = rng.standard_normal((2, in_dim)).astype(np.float32)
+    W = synth.weight_bf16(41, out_dim, (out_dim, in_dim), std=0.02)
+    b = synth.weight_bf16(42, out_dim, (out_dim,), std=0.02)
+    act = odit.silu(x) if silu_in else x
+    w64 = synth.bf16_bits_to_f32(W).astype(np.float64)
+    exact = act.astype(np.float64) @ w64.T + synth.bf16_bits_to_f32(b).astype(np.float64)
+    bound = 1e-5 * (np.abs(act).astype(np.float64) @ np.abs(w64).T) + 1e-6
+    for call in range(2):
+        y = qi.gemv(f32_tensor(x), bf16_tensor(W), bf16_tensor(b), silu_in).cpu().numpy()
+        err = np.abs(y.astype(np.float64) - exact)
+        assert (err <= bound).all(), f"call {call}: max error {err.max():.3e}"
+    assert_close(y, odit.linear(act, W, b), f"gemv {in_dim}->{out_dim}")
+
+
 # ---------------------------------------------------------------- GEMM
 
 @pytest.mark.parametrize("M,N,K", [(1, 256, 64), (200, 512, 256), (300, 768, 4096), (129, 256, 12288)])
