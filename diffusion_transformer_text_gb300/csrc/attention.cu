@@ -10,45 +10,41 @@
 //
 // Work unit = 128 query rows of one head. A persistent grid (one CTA per SM)
 // walks the units head-major, so the CTAs running at one time share a few heads'
-// K/V in L2. Tensor memory (512 columns):
-//   [0,128) O, [128,192) and [192,256) two Q slots (fp16 pairs, the A operand
-//   of Q K^T), [256,384) S, [384,448) and [448,512) two P buffers (fp16 pairs,
-//   the A operand of P V).
-// Q sits in tensor memory, so Q K^T reads only K from shared memory (shared
-// memory bandwidth, not the tensor core, is what a second operand stream from
-// shared memory would saturate). P has buffers of its own, so S(j+1) only
-// waits for the softmax warps to have read S(j) into registers, not for
-// P(j) V(j): the Q K^T of the next tile runs under the softmax of this one.
+// K/V in L2. Each key tile's 128 keys are split in two halves, and each half
+// keeps its own online softmax: its own running maximum, row sum and output
+// accumulator O_h over the keys of that half of every tile. The two halves never
+// wait for each other; the epilogue merges them (O = (O_0 a_0 + O_1 a_1) /
+// (l_0 a_0 + l_1 a_1) with a_h = 2^(m_h - max(m_0, m_1))), as a split over keys
+// is merged. Tensor memory (512 columns):
+//   [0,128) O_0, [128,256) O_1, [256,384) S, [384,448) and [448,512) two P
+//   buffers (fp16 pairs, the A operand of P V; half h at +32 h).
+// Q sits in shared memory (a TMA tile, the A operand of Q K^T with K). P has
+// buffers of its own, so S(j+1) only waits for the softmax warps to have read
+// S(j) into registers, not for P(j) V(j).
 //
 // Two threads issue the MMAs: one Q K^T, one P V. A thread issuing an N = 128
 // MMA is held about as long as the MMA runs, and each of its barrier checks
 // leaves the tensor pipe idle, so with a single issuer the pipe ran dry between
-// groups; with two, one thread's waits overlap the other's MMAs. P(j) V(j)
-// waits for the softmax of tile j; the softmax writes P(j) once P(j-2) V(j-2)
-// has read that buffer. Across units nothing drains: the next unit's Q is
-// loaded into the other Q slot during the current unit, its Q K^T start as
-// soon as S is read, and only its first P V waits for the epilogue to have read O.
+// groups; with two, one thread's waits overlap the other's MMAs. P_h(j) V_h(j)
+// (four MMAs into O_h) starts once half h has written P_h(j); half h writes
+// P_h(j) once P_h(j-2) V_h(j-2) has read that buffer.
 //
 // Roles (512 threads, four warpgroups):
-//   warp 0      TMA producer of the K tiles (ring of 3); warp 2 of the V tiles
+//   warp 0      TMA producer of the K tiles (ring of 3)
 //   warp 1      TMEM owner and Q K^T issuer; warp 3 P V issuer (one thread each)
+//   warp 2      TMA producer of the V tiles (ring of 2) and of each unit's Q tile,
+//               once the previous unit's last Q K^T has completed
 //   warps 4-11  softmax: warps 4-7 take keys 0-63 of every tile, warps 8-11
-//               keys 64-127. A thread holds one query row's half tile (the TMEM
-//               lane of its warp's quarter); the two halves of a row swap their maxima
-//               through shared memory (a two-warp mbarrier), so both take the
-//               tile's row maximum. The running max changes O only when it grows
-//               by more than 2^8 (each half rescales its 64 O columns after the
-//               previous P V has landed; the row sums use the same max, so the
-//               result is unchanged). Each half writes its P columns and keeps
-//               its own row sum.
-//   warps 12-15 Q loader and epilogue: thread = query row. Loads the next unit's
-//               Q rows into the free Q slot, then reads the finished unit's O,
-//               releases it and stores O / (sum of the two row sums) as fp16 (or
-//               MXFP8 codes and scales)
+//               keys 64-127; thread = one query row's half (the TMEM lane of its
+//               warp's quarter). A half's running max changes its O only when it
+//               grows by more than 2^8 (rescaled after that half's previous P V has
+//               landed; the row sum uses the same max, so the result is unchanged)
+//   warps 12-15 epilogue: thread = query row; merges the two halves' O and row
+//               sums and stores O as fp16 (or MXFP8 codes and scales)
 // The kernel launches at 128 registers a thread (four warps per SM sub-partition
 // at 16 K registers each); after set-up the first warpgroup gives registers back
-// (56) and the other three take them (152 each): 32 x (56 + 3 x 152) = 16 K per
-// sub-partition, the launch's whole allotment.
+// (104) and the other three take them (136 each): 32 x (104 + 3 x 136) = 16 K
+// per sub-partition, the launch's whole allotment.
 // Every mbarrier wait is bounded; on expiry the error word is set, the roles
 // leave their loops, the producers drain their loads and the issuers their MMAs
 // before TMEM is released.
@@ -61,47 +57,70 @@ namespace {
 constexpr int kBQ = 128;                       // query rows per unit
 constexpr int kBKV = 128;                      // keys per tile
 constexpr int kBox = 128 * 64 * 2;             // 128 rows x 64 dims: one 128-byte-swizzled TMA box (16 KB)
-constexpr int kTile = 2 * kBox;                // K or V tile: 128 keys x 128 dims (32 KB)
-constexpr int kStages = 3;                     // depth of the K ring and of the V ring
+constexpr int kTile = 2 * kBox;                // Q, K or V tile: 128 rows x 128 dims (32 KB)
+constexpr int kKStages = 3;                    // depth of the K ring
+constexpr int kVStages = 2;                    // depth of the V ring
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0;
-constexpr uint32_t kColQ = 128;
+constexpr uint32_t kColO = 0;                  // O_h at kColO + 128 h
 constexpr uint32_t kColS = 256;
-constexpr uint32_t kColP = 384;
-constexpr uint32_t kIdescQK = idesc_f16_f32(128, kBKV);      // A = Q (tensor memory), B = K (K-major)
+constexpr uint32_t kColP = 384;                // buffer b at kColP + 64 b, half h at + 32 h
+constexpr uint32_t kIdescQK = idesc_f16_f32(128, kBKV);      // A = Q, B = K (both K-major in shared memory)
 constexpr uint32_t kIdescPV = idesc_f16_f32_bmn(128, 128);   // A = P (tensor memory), B = V (MN-major)
-constexpr float kRescaleLog2 = 8.0f;           // rescale O only when the max grows by > 2^8
+constexpr float kRescaleLog2 = 8.0f;           // rescale O_h only when its max grows by > 2^8
 constexpr int kThreads = 512;
-constexpr uint32_t kRegsLow = 56;    // producers and MMA issuers
-constexpr uint32_t kRegsHigh = 152;  // softmax halves and epilogue
+constexpr uint32_t kRegsLow = 104;   // producers and MMA issuers
+constexpr uint32_t kRegsHigh = 136;  // softmax halves
+constexpr uint32_t kRegsEpi = 136;   // epilogue
+static_assert(kRegsLow + 2 * kRegsHigh + kRegsEpi == 4 * 128, "register split must equal the launch allotment");
+// setmaxnreg.dec may only lower and setmaxnreg.inc only raise the launch's 128
+static_assert(kRegsLow <= 128 && kRegsHigh >= 128 && kRegsEpi >= 128, "setmaxnreg direction");
 
 // mbarriers
 enum : int {
   kKFull = 0,
-  kKEmpty = kKFull + kStages,
-  kVFull = kKEmpty + kStages,
-  kVEmpty = kVFull + kStages,
-  kSFull = kVEmpty + kStages,  // S written
-  kSFree = kSFull + 1,         // S read into registers (8 softmax warps)
-  kPFull = kSFree + 1,         // [2] P buffer written (8 softmax warps)
-  kPvDone = kPFull + 2,        // [2] P V of the buffer's tile complete
-  kQFull = kPvDone + 2,        // [2] Q slot loaded (4 epilogue warps)
-  kQEmpty = kQFull + 2,        // [2] last Q K^T of the slot's unit complete
-  kOFull = kQEmpty + 2,        // unit's last P V complete
-  kOEmpty = kOFull + 1,        // O read by the epilogue (4 epilogue warps)
-  kLFull = kOEmpty + 1,        // [2] unit's row sums in shared memory (8 softmax warps)
-  kXchg = kLFull + 2,          // [2][4] row-max swap of the two halves, per tile parity and quarter (2 warps)
-  kDrainQK = kXchg + 8,
+  kKEmpty = kKFull + kKStages,
+  kVFull = kKEmpty + kKStages,
+  kVEmpty = kVFull + kVStages,
+  kQFull = kVEmpty + kVStages,  // unit's Q tile loaded
+  kQEmpty = kQFull + 1,         // unit's last Q K^T complete
+  kSFull = kQEmpty + 1,         // S written
+  kSFree = kSFull + 1,          // S read into registers (8 softmax warps)
+  kPFull = kSFree + 1,          // [buffer][half] P_h written (4 softmax warps)
+  kPvDone = kPFull + 4,         // [buffer][half] P_h V_h of the buffer's tile complete
+  kOFull = kPvDone + 4,         // unit's last P V complete
+  kOEmpty = kOFull + 1,         // O_0 and O_1 read by the epilogue (4 epilogue warps)
+  kLFull = kOEmpty + 1,         // unit's row sums and maxima in shared memory (8 softmax warps)
+  kDrainQK = kLFull + 1,
   kDrainPV = kDrainQK + 1,
   kNumBars = kDrainPV + 1
 };
-// shared memory after the K and V rings: barriers, TMEM address, abort flag,
-// row sums [2 units][2 halves][128 rows], half-tile maxima [2 tiles][2 halves][128 rows]
-constexpr int kSmem = 2 * kStages * kTile + 1024 + kNumBars * 8 + 16 + 2 * 2 * kBQ * 4 + 2 * 2 * kBQ * 4;
+__device__ __forceinline__ uint32_t bar_count(int i) {
+  if (i == kSFree || i == kLFull) return 8;
+  if ((i >= kPFull && i < kPFull + 4) || i == kOEmpty) return 4;
+  return 1;
+}
+// shared memory: Q tile, K ring, V ring, barriers, TMEM address, abort flag,
+// row sums and maxima [2 halves][128 rows] each
+constexpr int kSmem = (1 + kKStages + kVStages) * kTile + 1024 + kNumBars * 8 + 16 + 2 * 2 * kBQ * 4;
+static_assert(kSmem <= 227 * 1024, "shared memory over the per-block limit");
 
 struct Unit {
   int head, r0, ntiles;
 };
+
+// 32 fp32 values as fp16 at dst (16-byte aligned): four 16-byte stores
+__device__ __forceinline__ void store_o16(act_t* dst, const float (&v)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 w;
+    w.x = pack_f16x2(v[8 * i + 0], v[8 * i + 1]);
+    w.y = pack_f16x2(v[8 * i + 2], v[8 * i + 3]);
+    w.z = pack_f16x2(v[8 * i + 4], v[8 * i + 5]);
+    w.w = pack_f16x2(v[8 * i + 6], v[8 * i + 7]);
+    d[i] = w;
+  }
+}
 
 // Unit u: head u / nrt, query rows [r0, r0 + 128); key tiles to visit: image rows
 // need all Lk keys, a unit of text rows only the keys up to its last row.
@@ -115,25 +134,19 @@ __device__ __forceinline__ Unit unit_of(const AttnParams& p, int u, int nrt) {
   return x;
 }
 
-__device__ __forceinline__ bool mbar_count4(int i) {
-  return (i >= kQFull && i < kQFull + 2) || i == kOEmpty;
-}
-__device__ __forceinline__ bool mbar_count8(int i) {
-  return i == kSFree || (i >= kPFull && i < kPFull + 2) || (i >= kLFull && i < kLFull + 2);
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const AttnParams p,
-            float scale_log2) {
+    attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+            const __grid_constant__ CUtensorMap tmV, const AttnParams p, float scale_log2) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sK = smem;
-  uint8_t* sV = sK + kStages * kTile;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kStages * kTile);
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + kTile;
+  uint8_t* sV = sK + kKStages * kTile;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kVStages * kTile);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* lsum = reinterpret_cast<float*>(tmem_slot + 4);  // [2][2][kBQ]
-  float* hmax = lsum + 2 * 2 * kBQ;                       // [2][2][kBQ]
+  float* lsum = reinterpret_cast<float*>(tmem_slot + 4);  // [2][kBQ]
+  float* msum = lsum + 2 * kBQ;                           // [2][kBQ]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -141,12 +154,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = nrt * kHeads;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i)
-      mbar_init(&bars[i], mbar_count8(i) ? 8 : (mbar_count4(i) ? 4 : (i >= kXchg && i < kXchg + 8 ? 2 : 1)));
+    for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], bar_count(i));
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmQ);
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
   }
@@ -168,66 +181,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_release<kRegsLow>();
     if (lane != 0) {
       // one thread per warp works in this warpgroup
-    } else if (warp == 0 || warp == 2) {
-      // ---------------- TMA producers: warp 0 the K tiles, warp 2 the V tiles
-      const bool is_k = warp == 0;
-      uint64_t* full = bars + (is_k ? kKFull : kVFull);
-      uint64_t* empty = bars + (is_k ? kKEmpty : kVEmpty);
-      uint8_t* ring = is_k ? sK : sV;
-      const CUtensorMap* map = is_k ? &tmK : &tmV;
-      uint32_t t = 0;  // tiles issued by this thread
+    } else if (warp == 0) {
+      // ---------------- TMA producer of the K tiles
+      uint32_t t = 0;  // tiles issued
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
         const Unit un = unit_of(p, u, nrt);
         const int col0 = un.head * kHeadDim;
-        for (int j = 0; j < un.ntiles; ++j) {
-          const uint32_t st = t % kStages;
-          if (*abort_flag || !mbar_wait(&empty[st], ((t / kStages) & 1u) ^ 1u)) {
+        for (int j = 0; j < un.ntiles; ++j, ++t) {
+          const uint32_t st = t % kKStages;
+          if (*abort_flag || !mbar_wait(&bars[kKEmpty + st], ((t / kKStages) & 1u) ^ 1u)) {
             if (!*abort_flag) report_error(p.err, kErrTimeoutProducer);
             *abort_flag = 1;
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[st], kTile);
-          tma_load_2d(ring + st * kTile, map, &full[st], col0, j * kBKV);
-          tma_load_2d(ring + st * kTile + kBox, map, &full[st], col0 + 64, j * kBKV);
-          ++t;
+          mbar_arrive_expect_tx(&bars[kKFull + st], kTile);
+          tma_load_2d(sK + st * kTile, &tmK, &bars[kKFull + st], col0, j * kBKV);
+          tma_load_2d(sK + st * kTile + kBox, &tmK, &bars[kKFull + st], col0 + 64, j * kBKV);
         }
       }
       // every load this thread issued must land before the CTA may exit
-      for (uint32_t i = t > kStages ? t - kStages : 0; i < t; ++i)
-        if (!mbar_wait(&full[i % kStages], (i / kStages) & 1u)) report_error(p.err, kErrTimeoutDrain);
+      for (uint32_t i = t > kKStages ? t - kKStages : 0; i < t; ++i)
+        if (!mbar_wait(&bars[kKFull + i % kKStages], (i / kKStages) & 1u)) report_error(p.err, kErrTimeoutDrain);
+    } else if (warp == 2) {
+      // ---------------- TMA producer of the V tiles and of each unit's Q tile (once
+      // the previous unit's last Q K^T has completed)
+      uint32_t t = 0;  // V tiles issued
+      int nq = 0;      // Q tiles issued
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+        const Unit un = unit_of(p, u, nrt);
+        const int col0 = un.head * kHeadDim;
+        if (*abort_flag || (nq > 0 && !mbar_wait(&bars[kQEmpty], static_cast<uint32_t>(nq - 1) & 1u))) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&bars[kQFull], kTile);
+        tma_load_2d(sQ, &tmQ, &bars[kQFull], col0, un.r0);
+        tma_load_2d(sQ + kBox, &tmQ, &bars[kQFull], col0 + 64, un.r0);
+        ++nq;
+        for (int j = 0; j < un.ntiles; ++j, ++t) {
+          const uint32_t st = t % kVStages;
+          if (*abort_flag || !mbar_wait(&bars[kVEmpty + st], ((t / kVStages) & 1u) ^ 1u)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars[kVFull + st], kTile);
+          tma_load_2d(sV + st * kTile, &tmV, &bars[kVFull + st], col0, j * kBKV);
+          tma_load_2d(sV + st * kTile + kBox, &tmV, &bars[kVFull + st], col0 + 64, j * kBKV);
+        }
+      }
+      if (!ok) {
+        if (!*abort_flag) report_error(p.err, kErrTimeoutProducer);
+        *abort_flag = 1;
+      }
+      for (uint32_t i = t > kVStages ? t - kVStages : 0; i < t; ++i)
+        if (!mbar_wait(&bars[kVFull + i % kVStages], (i / kVStages) & 1u)) report_error(p.err, kErrTimeoutDrain);
+      // the last Q load (a completed phase reads as complete until the barrier
+      // moves on, and nothing else loads)
+      if (nq > 0 && !mbar_wait(&bars[kQFull], static_cast<uint32_t>(nq - 1) & 1u))
+        report_error(p.err, kErrTimeoutDrain);
     } else if (warp == 1) {
       // ---------------- Q K^T issuer: S(t) = Q K(t)^T, once the softmax warps have
       // read S(t - 1)
-      // descriptor of stage 0's K tile; the others differ in the start address field
+      const uint64_t qdesc = sw128_kmajor_desc(smem_u32(sQ));
       const uint64_t kdesc0 = sw128_kmajor_desc(smem_u32(sK));
       uint32_t t = 0;
       int ku = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total; u += gridDim.x, ++ku) {
         const Unit un = unit_of(p, u, nrt);
-        const uint32_t qs = static_cast<uint32_t>(ku) & 1u;
-        ok = !*abort_flag && mbar_wait(&bars[kQFull + qs], (static_cast<uint32_t>(ku) >> 1) & 1u);
+        ok = !*abort_flag && mbar_wait(&bars[kQFull], static_cast<uint32_t>(ku) & 1u);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t tQ = tmem + kColQ + qs * 64;
         for (int j = 0; j < un.ntiles; ++j, ++t) {
-          const uint32_t st = t % kStages;
-          ok = (t < 1 || mbar_wait(&bars[kSFree], (t - 1) & 1u)) && mbar_wait(&bars[kKFull + st], (t / kStages) & 1u);
+          const uint32_t st = t % kKStages;
+          ok = (t < 1 || mbar_wait(&bars[kSFree], (t - 1) & 1u)) &&
+               mbar_wait(&bars[kKFull + st], (t / kKStages) & 1u);
           if (!ok) break;
           tc_fence_after();
           const uint64_t kd = kdesc0 + ((st * kTile) >> 4);
 #pragma unroll
-          for (int k = 0; k < kHeadDim / 16; ++k)
-            mma_ts(tmem + kColS, tQ + k * 8, kd + (((k >> 2) * kBox + (k & 3) * 32) >> 4), kIdescQK,
-                   k > 0 ? 1u : 0u);
+          for (int k = 0; k < kHeadDim / 16; ++k) {
+            const uint32_t off = static_cast<uint32_t>(((k >> 2) * kBox + (k & 3) * 32) >> 4);
+            mma_ss(tmem + kColS, qdesc + off, kd + off, kIdescQK, k > 0 ? 1u : 0u);
+          }
           mma_commit(&bars[kSFull]);
           mma_commit(&bars[kKEmpty + st]);
         }
         if (!ok) break;
-        // the Q slot is free once the unit's last Q K^T has completed
-        mma_commit(&bars[kQEmpty + qs]);
+        // the Q tile is free once the unit's last Q K^T has completed
+        mma_commit(&bars[kQEmpty]);
       }
       if (!ok) {
         report_error(p.err, kErrTimeoutMma);
@@ -236,8 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bars[kDrainQK]);
       if (!mbar_wait(&bars[kDrainQK], 0)) report_error(p.err, kErrTimeoutDrain);
     } else {
-      // ---------------- P V issuer: O (+)= P(tt) V(tt); the first tile of a unit
-      // overwrites O once the epilogue has read the previous unit's
+      // ---------------- P V issuer: O_h (+)= P_h(t) V_h(t) for each half h (keys 64 h
+      // .. 64 h + 63 of the tile); the first tile of a unit overwrites O_0 and O_1
+      // once the epilogue has read the previous unit's
       const uint64_t vdesc0 = sw128_mnmajor_desc(smem_u32(sV), kBox, 1024);
       uint32_t t = 0;
       int ku = 0;
@@ -250,19 +296,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit un = unit_of(p, u, nrt);
         for (int j = 0; j < un.ntiles; ++j, ++t) {
           const uint32_t b = t & 1u;
-          const uint32_t st = t % kStages;
-          ok = mbar_wait(&bars[kPFull + b], (t >> 1) & 1u) &&
-               (j > 0 || ku == 0 || mbar_wait(&bars[kOEmpty], static_cast<uint32_t>(ku - 1) & 1u)) &&
-               mbar_wait(&bars[kVFull + st], (t / kStages) & 1u);
+          const uint32_t st = t % kVStages;
+          ok = (j > 0 || ku == 0 || mbar_wait(&bars[kOEmpty], static_cast<uint32_t>(ku - 1) & 1u)) &&
+               mbar_wait(&bars[kVFull + st], (t / kVStages) & 1u);
           if (!ok) break;
-          tc_fence_after();
           const uint64_t vd = vdesc0 + ((st * kTile) >> 4);
+          for (int h = 0; h < 2; ++h) {
+            ok = mbar_wait(&bars[kPFull + b * 2 + h], (t >> 1) & 1u);
+            if (!ok) break;
+            tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < kBKV / 16; ++k)
-            // P columns: 16 keys = 8 columns of fp16 pairs; V rows: 16 keys = 2 KB
-            mma_ts(tmem + kColO, tmem + kColP + b * 64 + k * 8, vd + ((k * 2048) >> 4), kIdescPV,
-                   (j > 0 || k > 0) ? 1u : 0u);
-          mma_commit(&bars[kPvDone + b]);
+            for (int k = 0; k < 4; ++k)
+              // P columns: 16 keys = 8 columns of fp16 pairs; V rows: 16 keys = 2 KB
+              mma_ts(tmem + kColO + 128u * h, tmem + kColP + b * 64 + h * 32 + k * 8,
+                     vd + ((static_cast<uint32_t>(4 * h + k) * 2048) >> 4), kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
+            mma_commit(&bars[kPvDone + b * 2 + h]);
+          }
+          if (!ok) break;
           mma_commit(&bars[kVEmpty + st]);
         }
         if (!ok) break;
@@ -276,12 +326,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 12) {
     regs_acquire<kRegsHigh>();
     // ---------------- softmax: warps 4..7 keys 0-63, warps 8..11 keys 64-127 of every
-    // tile; thread = one query row's half
+    // tile; thread = one query row's half, with its own max, row sum and O_h
     const int h = warp >= 8 ? 1 : 0;
     const int quarter = warp & 3;
     const int rit = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tO = tmem + lane_off + kColO + h * 64;  // this half's 64 O columns
+    const uint32_t tO = tmem + lane_off + kColO + 128u * h;
     const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
     uint32_t t = 0;
     int ku = 0;
@@ -299,12 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(&bars[kSFull], tt & 1u));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t tS = tmem + lane_off + kColS;
         // this half's 64 S columns: two loads in flight, one wait; then S may be
         // overwritten by the next tile's Q K^T
         uint32_t r[2][32];
-        tmem_ld32(tS + h * 64, r[0]);
-        tmem_ld32(tS + h * 64 + 32, r[1]);
+        tmem_ld32(tmem + lane_off + kColS + h * 64, r[0]);
+        tmem_ld32(tmem + lane_off + kColS + h * 64 + 32, r[1]);
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
@@ -324,39 +373,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; i += 2)
             mx4[(i >> 1) & 3] = fmax3(mx4[(i >> 1) & 3], __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
-        // swap half maxima with the warp that holds the row's other half
-        float* hm = hmax + (tt & 1u) * 2 * kBQ;
-        hm[h * kBQ + rit] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        __syncwarp();
-        uint64_t* xb = &bars[kXchg + (tt & 1u) * 4 + quarter];
-        if (lane == 0) mbar_arrive(xb);
-        ok = __all_sync(0xffffffffu, mbar_wait(xb, (tt >> 1) & 1u));
-        if (!ok) break;
-        tc_fence_after();
-        // the tile's row maximum in base-2 units (scale > 0 keeps the order); the
-        // same value in both halves
-        const float mx = fmaxf(hm[rit], hm[kBQ + rit]) * scale_log2;
+        // this half's maximum in base-2 units (scale > 0 keeps the order)
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
         const float m_new = fmaxf(m_used, mx);
         if (j == 0) {
           m_used = m_new;
         } else {
-          // A row whose maximum grew by more than 2^8 brings O and its row sum to the
-          // new maximum, once P V of the previous tile -- which may still be adding
-          // into O -- is done. tcgen05.ld/st must be executed by the whole warp, so
-          // the warp runs them if any row needs it; the other rows scale by exactly 1
-          // and keep their maximum, so a row's result never depends on which rows
-          // share its warp.
+          // A row whose maximum grew by more than 2^8 brings O_h and its row sum to
+          // the new maximum, once P_h V_h of the previous tile -- which may still be
+          // adding into O_h -- is done. tcgen05.ld/st must be executed by the whole
+          // warp, so the warp runs them if any row needs it; the other rows scale by
+          // exactly 1 and keep their maximum, so a row's result never depends on which
+          // rows share its warp. (A half whose keys so far were all masked has
+          // m_used = -inf and O_h = 0: it takes the first finite maximum.)
           const bool mine = m_new > m_used + kRescaleLog2;
           if (__any_sync(0xffffffffu, mine)) {
             const uint32_t tp = tt - 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&bars[kPvDone + (tp & 1u)], (tp >> 1) & 1u))) {
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(&bars[kPvDone + (tp & 1u) * 2 + h], (tp >> 1) & 1u))) {
               ok = false;
               break;
             }
             tc_fence_after();
             const float alpha = mine ? fast_exp2(m_used - m_new) : 1.0f;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 8; ++c) {
               uint32_t o[16];
               tmem_ld16(tO + c * 16, o);
               tmem_ld_wait();
@@ -370,20 +411,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        // P = 2^(s * scale - m) as fp16 pairs: this half's 64 keys go to columns
-        // 32 h .. 32 h + 31 of P buffer tt % 2 (masked keys give 2^-inf = 0), once
-        // P V of tile tt - 2 has read that buffer
-        if (tt >= 2) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&bars[kPvDone + b], ((tt - 2) >> 1) & 1u));
-          if (!ok) break;
-          tc_fence_after();
-        }
-        const uint32_t tP = tmem + lane_off + kColP + b * 64;
-        const uint64_t nm2 = f2_pack(-m_used, -m_used);
+        // P_h = 2^(s * scale - m) as fp16 pairs (masked keys give 2^-inf = 0; a half
+        // with no visible key yet subtracts 0 instead of -inf)
+        const float base = m_used == -INFINITY ? 0.f : m_used;
+        const uint64_t nm2 = f2_pack(-base, -base);
         uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
+        uint32_t pk[2][16];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const uint64_t x2 =
@@ -393,10 +428,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float e0 = fast_exp2(x0);
             const float e1 = fast_exp2(x1);
             rs2[i & 3] = add_f32x2(rs2[i & 3], f2_pack(e0, e1));
-            pk[i] = pack_f16x2(e0, e1);
+            pk[c][i] = pack_f16x2(e0, e1);
           }
-          tmem_st16(tP + h * 32 + c * 16, pk);
         }
+        // P buffer b is free once P_h V_h of tile tt - 2 has read it
+        if (tt >= 2) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars[kPvDone + b * 2 + h], ((tt - 2) >> 1) & 1u));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const uint32_t tP = tmem + lane_off + kColP + b * 64 + h * 32;
+        tmem_st16(tP, pk[0]);
+        tmem_st16(tP + 16, pk[1]);
         float s[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) f2_unpack(rs2[i], s[2 * i], s[2 * i + 1]);
@@ -404,11 +447,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         const bool last = j + 1 == un.ntiles;
-        if (last) lsum[((ku & 1) * 2 + h) * kBQ + rit] = l;
+        if (last) {
+          // the row sums' slots are free once the epilogue has read the previous
+          // unit's (it cannot yet have read this unit's O, so the wait is for that phase)
+          if (ku > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars[kOEmpty], static_cast<uint32_t>(ku - 1) & 1u));
+            if (!ok) break;
+          }
+          lsum[h * kBQ + rit] = l;
+          msum[h * kBQ + rit] = m_used;
+        }
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&bars[kPFull + b]);
-          if (last) mbar_arrive(&bars[kLFull + (ku & 1)]);
+          mbar_arrive(&bars[kPFull + b * 2 + h]);
+          if (last) mbar_arrive(&bars[kLFull]);
         }
       }
       if (!ok) break;
@@ -419,97 +471,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort_flag = 1;
     }
   } else {
-    regs_acquire<kRegsHigh>();
-    // ---------------- Q loader and epilogue (warps 12..15), thread = one query row
+    regs_acquire<kRegsEpi>();
+    // ---------------- epilogue (warps 12..15), thread = one query row: merges the
+    // two halves and stores O
     const int quarter = warp & 3;
     const int rit = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    // Q rows of unit u (fp16, 128 dims = 64 columns of pairs) into Q slot `slot`;
-    // rows past Rq are zero
-    auto load_q = [&](int u, uint32_t slot) {
-      const Unit un = unit_of(p, u, nrt);
-      const int row = un.r0 + rit;
-      const uint32_t dst = tmem + lane_off + kColQ + slot * 64;
-#pragma unroll
-      for (int hq = 0; hq < 2; ++hq) {
-        uint32_t v[32];
-        if (row < p.Rq) {
-          const uint4* src =
-              reinterpret_cast<const uint4*>(p.q + static_cast<size_t>(row) * kHidden + un.head * kHeadDim) + hq * 8;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 w = src[i];
-            v[i * 4 + 0] = w.x;
-            v[i * 4 + 1] = w.y;
-            v[i * 4 + 2] = w.z;
-            v[i * 4 + 3] = w.w;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0u;
-        }
-        tmem_st32(dst + hq * 32, v);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kQFull + slot]);
-    };
     bool ok = true;
     int ku = 0;
-    if (static_cast<int>(blockIdx.x) < total) load_q(blockIdx.x, 0);
-    for (int u = blockIdx.x; u < total; u += gridDim.x, ++ku) {
+    for (int u = blockIdx.x; ok && u < total; u += gridDim.x, ++ku) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      // the next unit's Q goes into the other slot once its previous unit's Q K^T are done
-      const int un_next = u + static_cast<int>(gridDim.x);
-      if (un_next < total) {
-        const uint32_t ns = static_cast<uint32_t>(ku + 1) & 1u;
-        if (ku + 1 >= 2) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&bars[kQEmpty + ns], (static_cast<uint32_t>(ku - 1) >> 1) & 1u));
-          if (!ok) break;
-        }
-        load_q(un_next, ns);
-      }
       ok = __all_sync(0xffffffffu, mbar_wait(&bars[kOFull], static_cast<uint32_t>(ku) & 1u)) &&
-           __all_sync(0xffffffffu, mbar_wait(&bars[kLFull + (ku & 1)], (static_cast<uint32_t>(ku) >> 1) & 1u));
+           __all_sync(0xffffffffu, mbar_wait(&bars[kLFull], static_cast<uint32_t>(ku) & 1u));
       if (!ok) break;
       tc_fence_after();
       const Unit un = unit_of(p, u, nrt);
-      const float l = lsum[((ku & 1) * 2) * kBQ + rit] + lsum[((ku & 1) * 2 + 1) * kBQ + rit];
-      uint32_t o[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + kColO + c * 32, o[c]);
-      tmem_ld_wait();
-      // O is in registers: the next unit's first P V may overwrite it
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kOEmpty]);
+      const float m0 = msum[rit], m1 = msum[kBQ + rit];
+      // half 0 sees key 0 in the first tile, so m0 is finite; a half with no
+      // visible key has m1 = -inf and weight 0
+      const float mm = fmaxf(m0, m1);
+      const float a0 = fast_exp2(m0 - mm);
+      const float a1 = fast_exp2(m1 - mm);
+      const float den = lsum[rit] * a0 + lsum[kBQ + rit] * a1;
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      const float w0 = a0 * inv, w1 = a1 * inv;
       const int row = un.r0 + rit;
-      if (row < p.Rq) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const int col0 = un.head * kHeadDim;
+      const int col0 = un.head * kHeadDim;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o0[32], o1[32];
+        tmem_ld32(tmem + lane_off + kColO + c * 32, o0);
+        tmem_ld32(tmem + lane_off + kColO + 128 + c * 32, o1);
+        tmem_ld_wait();
+        if (c == 3) {
+          // O_0 and O_1 are in registers: the next unit's first P V may overwrite them
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kOEmpty]);
+        }
+        if (row < p.Rq) {
+          float ov[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+          for (int i = 0; i < 32; ++i) ov[i] = __uint_as_float(o0[i]) * w0 + __uint_as_float(o1[i]) * w1;
           if (p.oq) {
             // MXFP8: these 32 O columns are one block of the out-projection's A operand
-            float ov[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __uint_as_float(o[c][i]) * inv;
             const int rg = p.oq_row0 + row;
             const int kcol = col0 + c * 32;
             p.osf[mx_sf_offset(rg, kcol / 32, p.oq_groups)] =
                 mx_quant32(ov, p.oq + static_cast<size_t>(rg) * kHidden + kcol);
           } else {
-            uint4* d4 = reinterpret_cast<uint4*>(p.o + static_cast<size_t>(row) * kHidden + col0 + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint4 w;
-              w.x = pack_f16x2(__uint_as_float(o[c][8 * i + 0]) * inv, __uint_as_float(o[c][8 * i + 1]) * inv);
-              w.y = pack_f16x2(__uint_as_float(o[c][8 * i + 2]) * inv, __uint_as_float(o[c][8 * i + 3]) * inv);
-              w.z = pack_f16x2(__uint_as_float(o[c][8 * i + 4]) * inv, __uint_as_float(o[c][8 * i + 5]) * inv);
-              w.w = pack_f16x2(__uint_as_float(o[c][8 * i + 6]) * inv, __uint_as_float(o[c][8 * i + 7]) * inv);
-              d4[i] = w;
-            }
+            store_o16(p.o + static_cast<size_t>(row) * kHidden + col0 + c * 32, ov);
           }
         }
       }
@@ -552,15 +563,16 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
   // Q is read and O written with 16-byte vector accesses; K and V come by TMA
   if ((reinterpret_cast<uintptr_t>(p.q) & 15) != 0 || (reinterpret_cast<uintptr_t>(p.o) & 15) != 0)
     return cudaErrorInvalidValue;
-  CUtensorMap mk, mv;
-  if (!encode_map16(&mk, p.k, p.Lk, kHidden, kBKV, false) || !encode_map16(&mv, p.v, p.Lk, kHidden, kBKV, false))
+  CUtensorMap mq, mk, mv;
+  if (!encode_map16(&mq, p.q, p.Rq, kHidden, kBQ, false) || !encode_map16(&mk, p.k, p.Lk, kHidden, kBKV, false) ||
+      !encode_map16(&mv, p.v, p.Lk, kHidden, kBKV, false))
     return cudaErrorInvalidValue;
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kHeadDim));
   const int units = ((p.Rq + kBQ - 1) / kBQ) * kHeads;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidValue;
   const int grid = units < sms ? units : sms;
-  return launch_dependent(attn_tc, dim3(grid), dim3(kThreads), kSmem, stream, mk, mv, p, scale_log2);
+  return launch_dependent(attn_tc, dim3(grid), dim3(kThreads), kSmem, stream, mq, mk, mv, p, scale_log2);
 }
 
 }  // namespace qi
