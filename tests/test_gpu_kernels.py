@@ -139,6 +139,24 @@ def test_attention_image_only_equals_joint(qi):
     assert np.array_equal(joint[:L], txt)
 
 
+def test_attention_consecutive_short_units(qi):
+    """A CTA that runs several one-key-tile units in a row: with 2400 query rows a head
+    has 19 row units, so on 152 SMs (608 units, 4 per CTA) a CTA whose first unit is a
+    head's rows 0..127 gets the first units of four heads; with L = 400 those rows are
+    text rows whose keys end inside the first key tile. Each unit's row sums must not be
+    overwritten before the previous unit's output is stored. Sampled rows against the
+    oracle: the first unit's, other text rows, and image rows."""
+    L, N = 400, 2000
+    R = L + N
+    q, k, v = _qkv(R, 17)
+    o = qi.attention(f16_tensor(q), f16_tensor(k), f16_tensor(v), L)
+    got = f16_bits_to_f32(o.cpu().numpy())
+    rows = np.array([0, 1, 31, 64, 127, 128, 200, 255, 399, 400, 401, 1200, 2047, R - 1])
+    ref = oatt.attention_rows(q[rows].reshape(len(rows), 32, 128), rows, k.reshape(R, 32, 128),
+                              v.reshape(R, 32, 128), L)
+    assert_close(got[rows], ref, "attention L=400 N=2000 sampled rows")
+
+
 def test_attention_long_keys(qi):
     """Several query and key tiles with a ragged tail at a realistic head count."""
     L, N = 407, 600
